@@ -1,0 +1,157 @@
+/*
+ * libqmm: block-quantized weight matmul for one GB300 GPU (sm_103a).
+ *
+ *     y[m, n] = sum_k dequant(W)[n, k] * x[m, k]
+ *
+ * The weights stay quantized in device memory and are dequantized on the fly inside the kernels: each
+ * weight block is read, dequantized and multiplied by the activation rows of a token tile (candle PR 4056,
+ * "Metal: 64-token tile for the quantized matrix-matrix kernel", section "Why the tile sets the weight
+ * reuse"). The expert-indexed form computes one mat-vec per routed (token, expert) pair (llama.cpp PR
+ * 28086, "metal : fix idle threads in mul_mv_iq3_xxs for ne00 < 1024", MUL_MAT_ID).
+ *
+ * Weight types and block layouts: QMM_F32 ... QMM_A4G64 below. The layouts are this library's own block
+ * format specification (the pages name the types but do not define them); each block stores a scale (and
+ * for some types a minimum or bias) plus packed integer codes, and row n of an N x K matrix is K/QK blocks
+ * stored back to back, rows following each other without padding.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named wq, x, y, ids, w_out, w_in are DEVICE pointers owned by the caller. The library
+ *     keeps no reference to them after the call returns and frees nothing it did not allocate.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Every call is asynchronous on it:
+ *     a return value of 0 means the work was launched, not that it finished.
+ *   - Return values: 0 on success, a negative QMM_E* code otherwise (qmm_strerror() names it). On any
+ *     error nothing is launched. Arguments are checked on the host without dereferencing device memory.
+ *   - wq, x and y must be 16-byte aligned.
+ *   - Nothing here is thread-safe against concurrent calls that share an output buffer.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Weight types (block size QK in weights / bytes per block). */
+enum qmm_type {
+    QMM_F32 = 0,   /*   1 /   4  plain binary32 */
+    QMM_F16 = 1,   /*   1 /   2  plain binary16 */
+    QMM_BF16 = 2,  /*   1 /   2  plain bfloat16 */
+    QMM_Q4_0 = 3,  /*  32 /  18  w = d*(q-8) */
+    QMM_Q4_1 = 4,  /*  32 /  20  w = d*q + m */
+    QMM_Q5_0 = 5,  /*  32 /  22  w = d*(q-16) */
+    QMM_Q5_1 = 6,  /*  32 /  24  w = d*q + m */
+    QMM_Q8_0 = 7,  /*  32 /  34  w = d*q */
+    QMM_Q2_K = 8,  /* 256 /  84  w = d*sc*q - dmin*mn, 16 sub-blocks of 16 */
+    QMM_Q3_K = 9,  /* 256 / 110  w = d*(sc-32)*(q-4), 16 sub-blocks of 16 */
+    QMM_Q4_K = 10, /* 256 / 144  w = d*sc*q - dmin*mn, 8 sub-blocks of 32 */
+    QMM_Q5_K = 11, /* 256 / 176  w = d*sc*q - dmin*mn, 8 sub-blocks of 32 */
+    QMM_Q6_K = 12, /* 256 / 210  w = d*sc*(q-32), 16 sub-blocks of 16 */
+    QMM_A4G64 = 13,/*  64 /  36  w = s*q + b, bf16 s and b (MLX-style group-64 affine 4-bit) */
+    QMM_NTYPES = 14
+};
+
+/* OR into `qtype` to pass bfloat16 activations instead of binary32. */
+#define QMM_X_BF16 0x100
+
+/* Error codes. */
+#define QMM_OK 0
+#define QMM_EQTYPE (-1)   /* unknown weight type or flag */
+#define QMM_EBLOCK (-2)   /* K is not a multiple of the type's block size */
+#define QMM_EDIM (-3)     /* a dimension is <= 0 or too large */
+#define QMM_ENULL (-4)    /* a required pointer is NULL */
+#define QMM_EALIGN (-5)   /* wq, x or y is not 16-byte aligned */
+#define QMM_ECUDA (-6)    /* a CUDA runtime call or launch failed */
+#define QMM_ERANGE (-7)   /* E, topk or a tile argument out of range */
+#define QMM_EWORKSPACE (-8) /* workspace missing or too small */
+
+/* Limits. */
+#define QMM_MAX_EXPERTS 256
+#define QMM_MAX_ID_SLOTS 4096 /* M * topk for qmm_id */
+
+/*
+ * qmm: y = x * dequant(W)^T.
+ *   wq    N x K weight matrix of type (qtype & 0xff), N * (K/QK) * bytes_per_block bytes.
+ *   x     M x K row-major activations, binary32, or bfloat16 when qtype has QMM_X_BF16.
+ *   y     M x N row-major binary32, overwritten.
+ * M <= 16 runs the memory-bound mat-vec path (all lanes on weights, narrow-K row split); larger M runs
+ * the tcgen05 tensor-core path with a 32/64/128-token tile picked by qmm_pick_tile(M). The tensor-core
+ * path rounds x and the dequantized weights to bfloat16 (round to nearest even) and accumulates in
+ * binary32; the mat-vec path multiplies the binary32 dequantized weights by x in binary32.
+ * The tensor-core path with binary32 x needs M*K*2 bytes of scratch for the bfloat16 copy of x; qmm()
+ * takes it from the stream-ordered allocator (cudaMallocAsync / cudaFreeAsync on `stream`). Callers
+ * that manage memory themselves use qmm_ws().
+ */
+int qmm(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, float *y, void *stream);
+
+/* Bytes of scratch qmm_ws() needs for these arguments (0 when none). */
+size_t qmm_workspace_size(int qtype, int64_t N, int64_t K, int64_t M);
+
+/* qmm() with caller-provided scratch: `workspace` is a device buffer of at least
+ * qmm_workspace_size(...) bytes, 256-byte aligned; may be NULL when that size is 0. */
+int qmm_ws(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, float *y,
+           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * qmm_id: expert-indexed mat-vec (MoE).  For each token t < M and slot j < topk, with e = ids[t*topk + j]:
+ *     y[(t*topk + j)*N + n] = sum_k dequant(W_e)[n, k] * x[t*K + k]
+ *   wq    HOST array of E device pointers, one N x K weight matrix of type qtype per expert
+ *         (each 16-byte aligned). The array itself is read during the call only.
+ *   ids   DEVICE int32 array, M x topk.
+ *   y     M x topk x N binary32, overwritten.
+ * Every distinct expert's rows are streamed once per call for all tokens routed to it. An id outside
+ * [0, E) cannot be checked on the host: that slot's output row is set to NaN and the device status word
+ * (qmm_get_status) records QMM_STATUS_BAD_ID. Limits: 1 <= E <= QMM_MAX_EXPERTS,
+ * 1 <= topk, M * topk <= QMM_MAX_ID_SLOTS.
+ */
+int qmm_id(const void *const *wq, int64_t E, int qtype, int64_t N, int64_t K, const void *x,
+           const int32_t *ids, int64_t M, int topk, float *y, void *stream);
+
+/*
+ * qmm_with_tile: qmm() with the path forced, for tests and diagnostics (mirrors the pages' explicit-tile
+ * entry point, candle PR 4056, section "What changes").
+ *   tile = 0       mat-vec path (any M; tokens are processed 16 at a time)
+ *   tile = 32/64/128  tensor-core path with that token tile
+ * Output is bit-identical across tile = 32, 64, 128 for the same inputs (same K order and the same
+ * split of K), which tests check.
+ */
+int qmm_with_tile(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, float *y,
+                  int tile, void *stream);
+
+/* The token-tile rule of the tensor-core path: the largest T in {32, 64, 128} whose padding
+ * ceil(M/T)*T - M equals the 32-token tile's, i.e. that pads no more tokens than the 32-token tile
+ * (candle PR 4056, section "Where the 64-token tile is used", extended to 128). Returns 0 for M <= 0. */
+int qmm_pick_tile(int64_t M);
+
+/* Which path qmm() takes for M tokens: 0 = mat-vec, 32/64/128 = tensor-core tile. */
+int qmm_pick_path(int qtype, int64_t N, int64_t K, int64_t M);
+
+/*
+ * qmm_dequant: w_out[n*K + k] = dequant(W)[n, k] as binary32. Each value is the exact value of the
+ * type's formula rounded once to binary32 (bit-exact against the oracle). w_out is N x K, 16-byte aligned.
+ */
+int qmm_dequant(const void *wq, int qtype, int64_t N, int64_t K, float *w_out, void *stream);
+
+/*
+ * qmm_quantize: encode an N x K binary32 matrix (device, row-major) into blocks of type qtype
+ * (deterministic round to nearest; decisions in binary32 so the result is reproducible bit for bit).
+ * wq_out must hold N * (K/QK) * bytes_per_block bytes. Not on the matmul path.
+ */
+int qmm_quantize(const float *w_in, int qtype, int64_t N, int64_t K, void *wq_out, void *stream);
+
+/* Block size in weights and bytes per block of a type (host only). */
+int qmm_type_info(int qtype, int *block_weights, int *block_bytes);
+
+/* Device status word, a bit set of QMM_STATUS_*: read (synchronising `stream`) and clear. */
+#define QMM_STATUS_BAD_ID 0x1    /* qmm_id met an expert id outside [0, E) */
+#define QMM_STATUS_TIMEOUT 0x2   /* a bounded wait in a tensor-core kernel gave up */
+int qmm_get_status(void *stream, unsigned int *status);
+
+const char *qmm_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QMM_H */

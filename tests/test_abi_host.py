@@ -1,0 +1,103 @@
+"""Host-side checks of the C-ABI library: it loads without a GPU, exports every function include/qmm.h
+declares, and rejects bad arguments with the documented codes before touching any device memory."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import weight_quantized_matmul_fly_gb300 as qmm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    qmm.build()
+    return qmm.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "qmm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(qmm[a-z_]*)\s*\(", src, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared()
+    assert "qmm" in names and "qmm_id" in names and len(names) >= 10
+    assert sorted(qmm.EXPORTS) == names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_type_info_table(L):
+    want = {"F32": (1, 4), "F16": (1, 2), "BF16": (1, 2), "Q4_0": (32, 18), "Q4_1": (32, 20), "Q5_0": (32, 22),
+            "Q5_1": (32, 24), "Q8_0": (32, 34), "Q2_K": (256, 84), "Q3_K": (256, 110), "Q4_K": (256, 144),
+            "Q5_K": (256, 176), "Q6_K": (256, 210), "A4G64": (64, 36)}
+    for t, v in want.items():
+        assert qmm.qmm_type_info(t) == v
+
+
+def test_strerror(L):
+    for c in range(-8, 1):
+        assert isinstance(qmm.qmm_strerror(c), str) and qmm.qmm_strerror(c) != "unknown error"
+
+
+P = ctypes.c_void_p
+A = 0x1000  # a 16-byte aligned fake address; never dereferenced: every call below fails its checks first
+
+
+@pytest.mark.parametrize("args,code", [
+    ((P(A), 14, 64, 64, P(A), 1, P(A), None), -1),           # bad type
+    ((P(A), 0x203, 64, 64, P(A), 1, P(A), None), -1),        # unknown flag bit
+    ((P(A), 3, 64, 48, P(A), 1, P(A), None), -2),            # K not a multiple of 32 for Q4_0
+    ((P(A), 10, 64, 512 + 32, P(A), 1, P(A), None), -2),     # K not a multiple of 256 for Q4_K
+    ((P(A), 3, 0, 64, P(A), 1, P(A), None), -3),             # N = 0
+    ((P(A), 3, 64, 64, P(A), 0, P(A), None), -3),            # M = 0
+    ((P(A), 3, 64, -32, P(A), 1, P(A), None), -3),           # K < 0
+    ((None, 3, 64, 64, P(A), 1, P(A), None), -4),            # null wq
+    ((P(A), 3, 64, 64, None, 1, P(A), None), -4),            # null x
+    ((P(A + 8), 3, 64, 64, P(A), 1, P(A), None), -5),        # misaligned wq
+    ((P(A), 3, 64, 64, P(A), 1, P(A + 4), None), -5),        # misaligned y
+])
+def test_qmm_argument_errors(L, args, code):
+    assert L.qmm(*args) == code
+
+
+def test_with_tile_bad_tile(L):
+    assert L.qmm_with_tile(P(A), 3, 64, 64, P(A), 40, P(A), 48, None) == -7
+
+
+def test_qmm_id_errors(L):
+    ptrs = (ctypes.c_void_p * 2)(A, A)
+    arr = ctypes.cast(ptrs, P)
+    assert L.qmm_id(arr, 0, 3, 64, 64, P(A), P(A), 1, 8, P(A), None) == -7          # E = 0
+    assert L.qmm_id(arr, 2, 3, 64, 64, P(A), P(A), 1000, 8, P(A), None) == -7       # M*topk too large
+    assert L.qmm_id(arr, 2, 3, 64, 48, P(A), P(A), 1, 8, P(A), None) == -2          # K
+    assert L.qmm_id(None, 2, 3, 64, 64, P(A), P(A), 1, 8, P(A), None) == -4
+    bad = (ctypes.c_void_p * 2)(A, A + 2)
+    assert L.qmm_id(ctypes.cast(bad, P), 2, 3, 64, 64, P(A), P(A), 1, 8, P(A), None) == -5
+
+
+def test_dequant_quantize_errors(L):
+    assert L.qmm_dequant(P(A), 20, 4, 64, P(A), None) == -1
+    assert L.qmm_dequant(P(A), 3, 4, 40, P(A), None) == -2
+    assert L.qmm_quantize(P(A), 3, 4, 64, None, None) == -4
+    assert L.qmm_quantize(P(A + 1), 3, 4, 64, P(A), None) == -5
+
+
+def test_pick_path(L):
+    # mat-vec up to 16 tokens, tensor-core tile above
+    assert qmm.qmm_pick_path("Q4_K", 4096, 2560, 1) == 0
+    assert qmm.qmm_pick_path("Q4_K", 4096, 2560, 16) == 0
+    assert qmm.qmm_pick_path("Q4_K", 4096, 2560, 17) == 32
+    assert qmm.qmm_pick_path("Q4_K", 4096, 2560, 2048) == 128
+    # plain type whose rows cannot be read by TMA stays on the mat-vec path
+    assert qmm.qmm_pick_path("F32", 64, 33, 512) == 0
+
+
+def test_workspace_size(L):
+    assert qmm.qmm_workspace_size("Q4_K", 4096, 2560, 1) == 0
+    assert qmm.qmm_workspace_size("Q4_K", 4096, 2560, 100) >= 100 * 2560 * 2
+    assert qmm.qmm_workspace_size("Q4_K", 4096, 2560, 100, x_bf16=True) == 0

@@ -1,0 +1,64 @@
+"""qmm_id (expert-indexed mat-vec) on the GPU against the oracle: K = 256 / 512 / 768 / 1024 (row split
+2 and 4, the plain mapping at 24 chunks), 1..24 tokens, top-8 of 16 experts (so experts are shared by
+several tokens), and out-of-range ids."""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+import weight_quantized_matmul_fly_gb300 as qmm
+from gpu_util import TOL_FP32, check_tol, dev, torch_cuda, x_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _experts(qtype, E, N, K, seed):
+    return [oracle.quantize(qtype, synthetic.weights(N, K, seed=seed + e)) for e in range(E)]
+
+
+def _run(wqs, qtype, N, K, x, ids):
+    torch = torch_cuda()
+    M, topk = ids.shape
+    y = torch.full((M, topk, N), float("nan"), dtype=torch.float32, device="cuda")
+    qmm.qmm_id([dev(w) for w in wqs], qtype, N, K, x_dev(x), dev(ids), y)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("K", [256, 512, 768, 1024])
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 12, 16, 24])
+def test_qmm_id_q4_0(K, M):
+    E, N, topk = 16, 200, 8
+    wqs = _experts("Q4_0", E, N, K, seed=K)
+    x = synthetic.activations(M, K, seed=M)
+    ids = synthetic.expert_ids(M, E=E, topk=topk, seed=M)
+    y = _run(wqs, "Q4_0", N, K, x, ids)
+    ref, bnd = oracle.qmm_id("Q4_0", wqs, N, K, x, ids)
+    check_tol(y, ref, bnd, TOL_FP32, "K=%d M=%d" % (K, M))
+
+
+@pytest.mark.parametrize("qtype", ["Q4_K", "Q6_K", "Q8_0", "A4G64"])
+def test_qmm_id_other_types(qtype):
+    E, N, K, M, topk = 8, 130, 1024, 6, 3
+    wqs = _experts(qtype, E, N, K, seed=50)
+    x = synthetic.activations(M, K, seed=2, bf16=(qtype == "A4G64"))
+    ids = synthetic.expert_ids(M, E=E, topk=topk, seed=2)
+    y = _run(wqs, qtype, N, K, x, ids)
+    ref, bnd = oracle.qmm_id(qtype, wqs, N, K, x, ids)
+    check_tol(y, ref, bnd, TOL_FP32, qtype)
+
+
+def test_qmm_id_duplicate_and_bad_ids():
+    torch_cuda()
+    E, N, K = 4, 70, 512
+    wqs = _experts("Q4_0", E, N, K, seed=9)
+    x = synthetic.activations(3, K, seed=9)
+    ids = np.array([[0, 0, 3], [2, 7, 1], [-1, 3, 3]], dtype=np.int32)
+    qmm.qmm_get_status()  # clear
+    y = _run(wqs, "Q4_0", N, K, x, ids)
+    st = qmm.qmm_get_status()
+    assert st & qmm.STATUS_BAD_ID
+    ref, bnd = oracle.qmm_id("Q4_0", wqs, N, K, x, ids)
+    check_tol(y, ref, bnd, TOL_FP32, "dup/bad ids")
+    assert np.all(np.isnan(y[1, 1])) and np.all(np.isnan(y[2, 0]))
+    assert qmm.qmm_get_status() == 0

@@ -1,0 +1,181 @@
+"""Python binding of libqmm, the block-quantized weight matmul for GB300 (sm_103a).
+
+Argument marshalling only: every function takes torch tensors (device memory owned by the caller),
+passes their pointers and the current CUDA stream to the C-ABI function of the same name (declared in
+include/qmm.h), and raises QmmError on a non-zero return code. All computation happens in the library's
+CUDA kernels; there is no other code path. If libqmm.so has not been built (``build()``), every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = ["QmmError", "TYPES", "TYPE_ID", "X_BF16", "build", "lib", "qmm", "qmm_ws", "qmm_workspace_size",
+           "qmm_id", "qmm_with_tile", "qmm_pick_tile", "qmm_pick_path", "qmm_dequant", "qmm_quantize",
+           "qmm_type_info", "qmm_get_status", "qmm_strerror", "row_bytes", "EXPORTS"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqmm.so")
+
+TYPES = ["F32", "F16", "BF16", "Q4_0", "Q4_1", "Q5_0", "Q5_1", "Q8_0",
+         "Q2_K", "Q3_K", "Q4_K", "Q5_K", "Q6_K", "A4G64"]
+TYPE_ID = {n: i for i, n in enumerate(TYPES)}
+X_BF16 = 0x100
+STATUS_BAD_ID, STATUS_TIMEOUT = 0x1, 0x2
+
+# Every symbol include/qmm.h declares.
+EXPORTS = ["qmm", "qmm_ws", "qmm_workspace_size", "qmm_id", "qmm_with_tile", "qmm_pick_tile", "qmm_pick_path",
+           "qmm_dequant", "qmm_quantize", "qmm_type_info", "qmm_get_status", "qmm_strerror"]
+
+
+class QmmError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__("%s failed: %s (%d)" % (what, qmm_strerror(code), code))
+        self.code = code
+
+
+def build(force: bool = False) -> str:
+    from . import buildlib as _b
+    return _b.build(force=force)
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libqmm (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libqmm.so is not built: run weight_quantized_matmul_fly_gb300.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I64, I, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+        sig = {
+            "qmm": ([P, I, I64, I64, P, I64, P, P], I),
+            "qmm_ws": ([P, I, I64, I64, P, I64, P, P, SZ, P], I),
+            "qmm_workspace_size": ([I, I64, I64, I64], SZ),
+            "qmm_id": ([P, I64, I, I64, I64, P, P, I64, I, P, P], I),
+            "qmm_with_tile": ([P, I, I64, I64, P, I64, P, I, P], I),
+            "qmm_pick_tile": ([I64], I),
+            "qmm_pick_path": ([I, I64, I64, I64], I),
+            "qmm_dequant": ([P, I, I64, I64, P, P], I),
+            "qmm_quantize": ([P, I, I64, I64, P, P], I),
+            "qmm_type_info": ([I, ctypes.POINTER(I), ctypes.POINTER(I)], I),
+            "qmm_get_status": ([P, ctypes.POINTER(ctypes.c_uint)], I),
+            "qmm_strerror": ([I], ctypes.c_char_p),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def _qt(qtype) -> int:
+    return TYPE_ID[qtype] if isinstance(qtype, str) else int(qtype)
+
+
+def _stream(stream):
+    if stream is not None:
+        return ctypes.c_void_p(int(stream))
+    import torch
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise QmmError(rc, what)
+
+
+def _xflag(x) -> int:
+    import torch
+    if x.dtype == torch.bfloat16:
+        return X_BF16
+    if x.dtype != torch.float32:
+        raise TypeError("activations must be float32 or bfloat16, got %s" % x.dtype)
+    return 0
+
+
+def qmm_strerror(code: int) -> str:
+    return lib().qmm_strerror(int(code)).decode()
+
+
+def qmm_type_info(qtype):
+    qk, nb = ctypes.c_int(), ctypes.c_int()
+    _check(lib().qmm_type_info(_qt(qtype), ctypes.byref(qk), ctypes.byref(nb)), "qmm_type_info")
+    return qk.value, nb.value
+
+
+def row_bytes(qtype, K: int) -> int:
+    qk, nb = qmm_type_info(qtype)
+    return (K // qk) * nb
+
+
+def qmm_pick_tile(M: int) -> int:
+    return lib().qmm_pick_tile(int(M))
+
+
+def qmm_pick_path(qtype, N: int, K: int, M: int) -> int:
+    return lib().qmm_pick_path(_qt(qtype), int(N), int(K), int(M))
+
+
+def qmm_workspace_size(qtype, N: int, K: int, M: int, x_bf16: bool = False) -> int:
+    return lib().qmm_workspace_size(_qt(qtype) | (X_BF16 if x_bf16 else 0), int(N), int(K), int(M))
+
+
+def qmm(wq, qtype, N: int, K: int, x, y, stream=None):
+    """y[M, N] = x[M, K] @ dequant(wq)^T (x float32 or bfloat16, y float32; all CUDA tensors)."""
+    M = x.shape[0]
+    rc = lib().qmm(_ptr(wq), _qt(qtype) | _xflag(x), int(N), int(K), _ptr(x), int(M), _ptr(y), _stream(stream))
+    _check(rc, "qmm")
+    return y
+
+
+def qmm_ws(wq, qtype, N: int, K: int, x, y, workspace, stream=None):
+    M = x.shape[0]
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().qmm_ws(_ptr(wq), _qt(qtype) | _xflag(x), int(N), int(K), _ptr(x), int(M), _ptr(y),
+                      _ptr(workspace), nbytes, _stream(stream))
+    _check(rc, "qmm_ws")
+    return y
+
+
+def qmm_with_tile(wq, qtype, N: int, K: int, x, y, tile: int, stream=None):
+    M = x.shape[0]
+    rc = lib().qmm_with_tile(_ptr(wq), _qt(qtype) | _xflag(x), int(N), int(K), _ptr(x), int(M), _ptr(y),
+                             int(tile), _stream(stream))
+    _check(rc, "qmm_with_tile")
+    return y
+
+
+def qmm_id(wqs, qtype, N: int, K: int, x, ids, y, stream=None):
+    """y[M, topk, N]: for each token t and slot j, x[t] @ dequant(wqs[ids[t, j]])^T."""
+    M, topk = ids.shape
+    arr = (ctypes.c_void_p * len(wqs))(*[w.data_ptr() for w in wqs])
+    rc = lib().qmm_id(ctypes.cast(arr, ctypes.c_void_p), len(wqs), _qt(qtype) | _xflag(x), int(N), int(K),
+                      _ptr(x), _ptr(ids), int(M), int(topk), _ptr(y), _stream(stream))
+    _check(rc, "qmm_id")
+    return y
+
+
+def qmm_dequant(wq, qtype, N: int, K: int, w_out, stream=None):
+    _check(lib().qmm_dequant(_ptr(wq), _qt(qtype), int(N), int(K), _ptr(w_out), _stream(stream)), "qmm_dequant")
+    return w_out
+
+
+def qmm_quantize(w_in, qtype, N: int, K: int, wq_out, stream=None):
+    _check(lib().qmm_quantize(_ptr(w_in), _qt(qtype), int(N), int(K), _ptr(wq_out), _stream(stream)),
+           "qmm_quantize")
+    return wq_out
+
+
+def qmm_get_status(stream=None) -> int:
+    v = ctypes.c_uint(0)
+    _check(lib().qmm_get_status(_stream(stream), ctypes.byref(v)), "qmm_get_status")
+    return v.value

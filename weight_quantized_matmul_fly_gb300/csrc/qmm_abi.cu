@@ -1,0 +1,232 @@
+// The C-ABI of libqmm: argument checks, path and tile choice, launches. No device memory is touched on
+// the host; every call is asynchronous on the caller's stream.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qmm.h"
+#include "qmm_common.cuh"
+
+namespace wqk {
+// The device status word (QMM_STATUS_* bits). Host code reaches it through status_ptr().
+__device__ unsigned int g_status = 0;
+
+int launch_gemv(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int64_t M, float *y,
+                cudaStream_t st);
+int launch_mm(int qt, int tile, const void *wq, int64_t N, int64_t K, const void *x_bf16, int64_t M, float *y,
+              unsigned int *status, cudaStream_t st);
+int launch_x_to_bf16(const float *x, void *out, int64_t n, cudaStream_t st);
+int launch_mvid(int qt, bool xbf16, const void *const *wq, int64_t E, int64_t N, int64_t K, const void *x,
+                const int32_t *ids, int64_t M, int topk, float *y, unsigned int *status, cudaStream_t st);
+int launch_dequant(int qt, const void *wq, int64_t N, int64_t K, float *out, cudaStream_t st);
+int launch_quantize(int qt, const float *w, int64_t N, int64_t K, void *out, cudaStream_t st);
+}  // namespace wqk
+
+using namespace wqk;
+
+namespace {
+
+constexpr int64_t kMaxDim = (int64_t)1 << 31;   // rows, columns and tokens each below 2^31
+constexpr int kGemvMaxM = 16;                   // mat-vec path up to here, tensor-core path above
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Common checks of qmm-family arguments. Returns 0 or a QMM_E* code.
+int check_qmm(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, const float *y) {
+    if ((qtype & ~(0xff | QMM_X_BF16)) != 0) return QMM_EQTYPE;
+    const int qt = qtype & 0xff;
+    if (qt < 0 || qt >= T_COUNT) return QMM_EQTYPE;
+    if (N <= 0 || K <= 0 || M <= 0 || N >= kMaxDim || K >= kMaxDim || M >= kMaxDim) return QMM_EDIM;
+    if (K % kQK[qt] != 0) return QMM_EBLOCK;
+    if (!wq || !x || !y) return QMM_ENULL;
+    if (!aligned16(wq) || !aligned16(x) || !aligned16(y)) return QMM_EALIGN;
+    return 0;
+}
+
+// The tensor-core path reads bf16 activation rows by TMA: their stride (K * 2 bytes) must be a multiple of
+// 16 bytes, and the decoders walk 32-weight chunks.
+inline bool mm_eligible(int qt, int64_t K) { return (K % 8) == 0 && (kQK[qt] >= 32 || K % 32 == 0); }
+
+// Device address of the status word on the current device (looked up once per device).
+unsigned int *status_ptr() {
+    static unsigned int *cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!cache[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<unsigned int *>(p);
+    }
+    return cache[dev];
+}
+
+inline size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+// Scratch the tensor-core path needs: a bf16 copy of binary32 activations.
+size_t ws_bytes(int qtype, int64_t K, int64_t M, int path) {
+    if (path == 0 || (qtype & QMM_X_BF16)) return 0;
+    return align256((size_t)M * (size_t)K * 2);
+}
+
+int run_mm(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, float *y, int tile,
+           void *ws, size_t wsb, cudaStream_t st) {
+    const int qt = qtype & 0xff;
+    const void *xb = x;
+    if (!(qtype & QMM_X_BF16)) {
+        const size_t need = ws_bytes(qtype, K, M, tile);
+        if (!ws || wsb < need) return QMM_EWORKSPACE;
+        if (reinterpret_cast<uintptr_t>(ws) & 255u) return QMM_EALIGN;
+        int rc = launch_x_to_bf16(static_cast<const float *>(x), ws, M * K, st);
+        if (rc) return rc;
+        xb = ws;
+    }
+    unsigned int *status = status_ptr();
+    if (!status) return QMM_ECUDA;
+    return launch_mm(qt, tile, wq, N, K, xb, M, y, status, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+int qmm_pick_tile(int64_t M) {
+    if (M <= 0) return 0;
+    const int64_t pad32 = (M + 31) / 32 * 32 - M;
+    int best = 32;
+    for (int T : {64, 128})
+        if ((M + T - 1) / T * T - M == pad32) best = T;
+    return best;
+}
+
+int qmm_pick_path(int qtype, int64_t N, int64_t K, int64_t M) {
+    (void)N;
+    const int qt = qtype & 0xff;
+    if (qt < 0 || qt >= T_COUNT) return QMM_EQTYPE;
+    if (M <= kGemvMaxM || !mm_eligible(qt, K)) return 0;
+    return qmm_pick_tile(M);
+}
+
+size_t qmm_workspace_size(int qtype, int64_t N, int64_t K, int64_t M) {
+    const int path = qmm_pick_path(qtype, N, K, M);
+    if (path <= 0) return 0;
+    return ws_bytes(qtype, K, M, path);
+}
+
+int qmm_ws(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, float *y, void *workspace,
+           size_t workspace_bytes, void *stream) {
+    int rc = check_qmm(wq, qtype, N, K, x, M, y);
+    if (rc) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int path = qmm_pick_path(qtype, N, K, M);
+    if (path == 0) return launch_gemv(qtype & 0xff, (qtype & QMM_X_BF16) != 0, wq, N, K, x, M, y, st);
+    return run_mm(wq, qtype, N, K, x, M, y, path, workspace, workspace_bytes, st);
+}
+
+int qmm(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, float *y, void *stream) {
+    int rc = check_qmm(wq, qtype, N, K, x, M, y);
+    if (rc) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int path = qmm_pick_path(qtype, N, K, M);
+    if (path == 0) return launch_gemv(qtype & 0xff, (qtype & QMM_X_BF16) != 0, wq, N, K, x, M, y, st);
+    const size_t need = ws_bytes(qtype, K, M, path);
+    void *ws = nullptr;
+    if (need) {
+        if (cudaMallocAsync(&ws, need, st) != cudaSuccess) return QMM_ECUDA;
+    }
+    rc = run_mm(wq, qtype, N, K, x, M, y, path, ws, need, st);
+    if (ws) cudaFreeAsync(ws, st);
+    return rc;
+}
+
+int qmm_with_tile(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, float *y, int tile,
+                  void *stream) {
+    int rc = check_qmm(wq, qtype, N, K, x, M, y);
+    if (rc) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (tile == 0) return launch_gemv(qtype & 0xff, (qtype & QMM_X_BF16) != 0, wq, N, K, x, M, y, st);
+    if (tile != 32 && tile != 64 && tile != 128) return QMM_ERANGE;
+    if (!mm_eligible(qtype & 0xff, K)) return QMM_EBLOCK;
+    const size_t need = ws_bytes(qtype, K, M, tile);
+    void *ws = nullptr;
+    if (need) {
+        if (cudaMallocAsync(&ws, need, st) != cudaSuccess) return QMM_ECUDA;
+    }
+    rc = run_mm(wq, qtype, N, K, x, M, y, tile, ws, need, st);
+    if (ws) cudaFreeAsync(ws, st);
+    return rc;
+}
+
+int qmm_id(const void *const *wq, int64_t E, int qtype, int64_t N, int64_t K, const void *x, const int32_t *ids,
+           int64_t M, int topk, float *y, void *stream) {
+    if ((qtype & ~(0xff | QMM_X_BF16)) != 0) return QMM_EQTYPE;
+    const int qt = qtype & 0xff;
+    if (qt < 0 || qt >= T_COUNT) return QMM_EQTYPE;
+    if (N <= 0 || K <= 0 || M <= 0 || N >= kMaxDim || K >= kMaxDim) return QMM_EDIM;
+    if (K % kQK[qt] != 0 || K % 32 != 0) return QMM_EBLOCK;
+    if (E < 1 || E > QMM_MAX_EXPERTS || topk < 1 || M * (int64_t)topk > QMM_MAX_ID_SLOTS) return QMM_ERANGE;
+    if (!wq || !x || !ids || !y) return QMM_ENULL;
+    for (int64_t e = 0; e < E; ++e) {
+        if (!wq[e]) return QMM_ENULL;
+        if (!aligned16(wq[e])) return QMM_EALIGN;
+    }
+    if (!aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(ids) & 3u)) return QMM_EALIGN;
+    unsigned int *status = status_ptr();
+    if (!status) return QMM_ECUDA;
+    return launch_mvid(qt, (qtype & QMM_X_BF16) != 0, wq, E, N, K, x, ids, M, topk, y, status,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int qmm_dequant(const void *wq, int qtype, int64_t N, int64_t K, float *w_out, void *stream) {
+    if (qtype < 0 || qtype >= T_COUNT) return QMM_EQTYPE;
+    if (N <= 0 || K <= 0 || N >= kMaxDim || K >= kMaxDim) return QMM_EDIM;
+    if (K % kQK[qtype] != 0) return QMM_EBLOCK;
+    if (!wq || !w_out) return QMM_ENULL;
+    if (!aligned16(wq) || !aligned16(w_out)) return QMM_EALIGN;
+    return launch_dequant(qtype, wq, N, K, w_out, static_cast<cudaStream_t>(stream));
+}
+
+int qmm_quantize(const float *w_in, int qtype, int64_t N, int64_t K, void *wq_out, void *stream) {
+    if (qtype < 0 || qtype >= T_COUNT) return QMM_EQTYPE;
+    if (N <= 0 || K <= 0 || N >= kMaxDim || K >= kMaxDim) return QMM_EDIM;
+    if (K % kQK[qtype] != 0) return QMM_EBLOCK;
+    if (!w_in || !wq_out) return QMM_ENULL;
+    if (!aligned16(w_in) || !aligned16(wq_out)) return QMM_EALIGN;
+    return launch_quantize(qtype, w_in, N, K, wq_out, static_cast<cudaStream_t>(stream));
+}
+
+int qmm_type_info(int qtype, int *block_weights, int *block_bytes) {
+    if (qtype < 0 || qtype >= T_COUNT) return QMM_EQTYPE;
+    if (!block_weights || !block_bytes) return QMM_ENULL;
+    *block_weights = kQK[qtype];
+    *block_bytes = kBytes[qtype];
+    return 0;
+}
+
+int qmm_get_status(void *stream, unsigned int *status) {
+    if (!status) return QMM_ENULL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned int zero = 0, v = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_status, sizeof(v), 0, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return QMM_ECUDA;
+    if (cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return QMM_ECUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return QMM_ECUDA;
+    *status = v;
+    return 0;
+}
+
+const char *qmm_strerror(int code) {
+    switch (code) {
+    case QMM_OK: return "ok";
+    case QMM_EQTYPE: return "unknown weight type or flag";
+    case QMM_EBLOCK: return "K is not a multiple of the block size";
+    case QMM_EDIM: return "dimension out of range";
+    case QMM_ENULL: return "null pointer";
+    case QMM_EALIGN: return "pointer not 16-byte aligned";
+    case QMM_ECUDA: return "CUDA launch or runtime error";
+    case QMM_ERANGE: return "E, topk or tile out of range";
+    case QMM_EWORKSPACE: return "workspace missing or too small";
+    default: return "unknown error";
+    }
+}
+
+}  // extern "C"

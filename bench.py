@@ -1,0 +1,425 @@
+"""Benchmark: one Qwen3-Embedding-4B-shaped layer of block-quantized matmuls on one GB300.
+
+A step is one pass of the whole hot path over the workload the pages time (candle PR 4056, "Metal:
+64-token tile for the quantized matrix-matrix kernel", section "This branch, kernel level"): the seven
+projections (attn_q/k/v/output Q4_K/Q6_K, ffn_gate/up Q4_K, ffn_down Q6_K) at every token count
+M in {1, 2, 7, 32, 33, 64, 96, 100, 128, 130, 136, 512, 2048}, plus the 65-token case as a batch of two
+sequences: 105 qmm calls. M <= 16 runs the mat-vec path, larger M the tcgen05 path.
+
+Metric: weight-GB/s of the M <= 16 calls against HBM (value), and TFLOPS of the M >= 64 calls against the
+bf16 tensor-core peak (tflops_m_ge_64). Inputs are resident in HBM; weights rotate through 7 copies of the
+layer (447 MB, more than 3x the 129 MB L2) so that no call reads weights another call left in L2.
+The e2e figure times the same calls through the C-ABI with activations copied from pinned host memory and
+results copied back inside the timed region.
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference] [--case NAME:M]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic  # noqa: E402
+
+METRIC = "qmatmul weight-GB/s vs HBM peak (M≤16); TFLOPS vs bf16 MMA peak (M≥64)"
+LAYER = synthetic.QWEN3_EMB_4B_LAYER
+TOKENS = synthetic.QWEN3_EMB_4B_TOKENS
+BATCH2 = synthetic.QWEN3_EMB_4B_BATCH2_TOKENS
+COPIES = 7
+BPW = {"Q4_K": 4.5, "Q6_K": 6.5625}
+WORKLOAD = ("Qwen3-Embedding-4B layer: attn_q 4096x2560 Q4_K, attn_k 1024x2560 Q4_K, attn_v 1024x2560 Q6_K, "
+            "attn_output 2560x4096 Q4_K, ffn_gate/ffn_up 9728x2560 Q4_K, ffn_down 2560x9728 Q6_K; "
+            "M in {1,2,7,32,33,64,96,100,128,130,136,512,2048} + 2x65; fp32 activations N(0,1), "
+            "weights N(0,0.02) quantized")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def calls_of_step():
+    """(name, N, K, qtype, M, batch_index) for one step, grouped by M so consecutive calls touch
+    different matrices."""
+    out = []
+    for M in TOKENS:
+        for name, N, K, qt in LAYER:
+            out.append((name, N, K, qt, M, 0))
+        if M == 64:  # the 65-token batch of two sits between 64 and 96 in token order
+            for b in range(2):
+                for name, N, K, qt in LAYER:
+                    out.append((name, N, K, qt, BATCH2, b))
+    return out
+
+
+def weight_bytes(N, K, qt):
+    return N * K * BPW[qt] / 8
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", "qmm_clocks_%d.csv" % os.getpid())
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if not self.proc or not os.path.exists(self.path):
+            return None
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [s.strip() for s in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = max(smax, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def max_over_ranks(pg, v, device=None):
+    if pg is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    import weight_quantized_matmul_fly_gb300 as qmm
+
+    world, rank, local, pg = dist_setup(args)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    qmm.build()
+    peaks = load_peaks()
+
+    calls = calls_of_step()
+    if args.case:
+        name, m = args.case.split(":")
+        calls = [c for c in calls if c[0] == name and c[4] == int(m) and c[5] == 0]
+        assert calls, "no such case"
+
+    # weights: 7 copies of the layer, quantized on the device from seeded binary32 weights
+    wq = {}
+    for copy in range(COPIES):
+        for name, N, K, qt in LAYER:
+            w32 = torch.from_numpy(synthetic.weights(N, K, seed=copy)).to(dev)
+            buf = torch.empty(qmm.row_bytes(qt, K) * N, dtype=torch.uint8, device=dev)
+            qmm.qmm_quantize(w32, qt, N, K, buf)
+            wq[(copy, name)] = buf
+            del w32
+    xs, ys = {}, {}
+    ws_bytes = 0
+    for name, N, K, qt, M, b in calls:
+        if (M, K, b) not in xs:
+            xs[(M, K, b)] = torch.from_numpy(synthetic.activations(M, K, seed=M + 17 * b)).to(dev)
+        if (M, N) not in ys:
+            ys[(M, N)] = torch.empty((M, N), dtype=torch.float32, device=dev)
+        ws_bytes = max(ws_bytes, qmm.qmm_workspace_size(qt, N, K, M))
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+    L = qmm.lib()
+    import ctypes
+    P = ctypes.c_void_p
+
+    def launches_of(M, K):
+        return 1 if qmm.qmm_pick_path("Q4_K", 1, K, M) == 0 else 2
+
+    ncalls = len(calls)
+    per_step_launches = sum(launches_of(c[4], c[2]) for c in calls)
+
+    # raw argument tuples (C-ABI calls, no Python tensor work inside the timed loop)
+    raw = []
+    for copy in range(COPIES):
+        row = []
+        for name, N, K, qt, M, b in calls:
+            row.append((P(wq[(copy, name)].data_ptr()), qmm.TYPE_ID[qt], N, K, P(xs[(M, K, b)].data_ptr()), M,
+                        P(ys[(M, N)].data_ptr()), P(ws.data_ptr()), ws.numel(), P(sptr)))
+        raw.append(row)
+
+    def one_step(step, ev=None):
+        r = raw[step % COPIES]
+        for i, a in enumerate(r):
+            if ev is not None:
+                ev[2 * i].record(stream)
+            rc = L.qmm_ws(*a)
+            if rc:
+                raise RuntimeError("qmm_ws: " + qmm.qmm_strerror(rc))
+            if ev is not None:
+                ev[2 * i + 1].record(stream)
+
+    for s in range(args.warmup):
+        one_step(s)
+    torch.cuda.synchronize()
+
+    # per-call events for a breakdown, recorded on the launching stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * ncalls)] for _ in range(args.steps)]
+    t0e = torch.cuda.Event(enable_timing=True)
+    t1e = torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        t0e.record(stream)
+        for s in range(args.steps):
+            one_step(args.warmup + s, evs[s])
+        t1e.record(stream)
+        torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    total_ms = max_over_ranks(pg, t0e.elapsed_time(t1e), dev)
+    per_call = np.zeros((args.steps, ncalls))
+    for s in range(args.steps):
+        for i in range(ncalls):
+            per_call[s, i] = evs[s][2 * i].elapsed_time(evs[s][2 * i + 1])
+    call_ms = per_call.mean(axis=0)
+
+    # aggregates
+    small = [i for i, c in enumerate(calls) if c[4] <= 16]
+    big = [i for i, c in enumerate(calls) if c[4] >= 64]
+    wb_small = sum(weight_bytes(calls[i][1], calls[i][2], calls[i][3]) for i in small)
+    t_small = sum(call_ms[i] for i in small) * 1e-3
+    fl_big = sum(2.0 * calls[i][4] * calls[i][1] * calls[i][2] for i in big)
+    t_big = sum(call_ms[i] for i in big) * 1e-3
+    gbs = wb_small / t_small / 1e9 * world if small else None
+    tfl = fl_big / t_big / 1e12 * world if big else None
+
+    # dominant call class by time: the tensor-core calls at M >= 512 (or the mat-vec ones)
+    dom = [i for i, c in enumerate(calls) if c[4] >= 512]
+    if dom and sum(call_ms[i] for i in dom) >= sum(call_ms[i] for i in small):
+        fl = sum(2.0 * calls[i][4] * calls[i][1] * calls[i][2] for i in dom)
+        t = sum(call_ms[i] for i in dom) * 1e-3
+        ach = fl / t / 1e12
+        roof = {"bound": "tensor", "kernel": "mm_kernel (tcgen05) incl. its bf16 activation pre-pass",
+                "calls": "M in {512, 2048}", "achieved": round(ach, 2), "peak": peaks["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops_sustained"], 4),
+                "peak_kind": "bf16 sustained, %s" % peaks["source"], "traffic": None,
+                "algorithmic_per_launch": "2*M*N*K flops"}
+    else:
+        ach = wb_small / t_small / 1e9
+        roof = {"bound": "hbm", "kernel": "gemv_kernel", "calls": "M in {1, 2, 7}", "achieved": round(ach, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
+                "peak_kind": "HBM copy, %s" % peaks["source"], "traffic": None,
+                "algorithmic_per_launch": "N*K*bpw/8 weight bytes"}
+
+    per_m = {}
+    for i, c in enumerate(calls):
+        key = "%dx%d" % (2, c[4]) if c[4] == BATCH2 else str(c[4])
+        d = per_m.setdefault(key, {"us": 0.0, "wbytes": 0.0, "flops": 0.0})
+        d["us"] += call_ms[i] * 1e3
+        d["wbytes"] += weight_bytes(c[1], c[2], c[3])
+        d["flops"] += 2.0 * c[4] * c[1] * c[2]
+    for k, d in per_m.items():
+        d["weight_gbs"] = round(d["wbytes"] / (d["us"] * 1e-6) / 1e9, 1)
+        d["tflops"] = round(d["flops"] / (d["us"] * 1e-6) / 1e12, 2)
+        d["us"] = round(d["us"], 2)
+        del d["wbytes"], d["flops"]
+
+    e2e = run_e2e(args, qmm, torch, dev, calls, wq, ws) if not args.case else None
+    cpu = cpu_baseline(args) if (rank == 0 and world == 1 and not args.no_cpu and not args.case) else None
+
+    clocks = clk.summary()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(gbs, 1) if gbs else None, "unit": "GB/s",
+            "tflops_m_ge_64": {"value": round(tfl, 2) if tfl else None, "unit": "TFLOP/s",
+                               "frac_of_bf16_sustained": round(tfl / peaks["bf16_tflops_sustained"], 4) if tfl else None},
+            "value_frac_of_hbm": round(gbs / peaks["hbm_gbs"] / world, 4) if gbs else None,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32 (M<=16) + bf16 in / f32 accumulate (M>16)", "data": "synthetic",
+            "config": {"workload": WORKLOAD if not args.case else "single call " + args.case,
+                       "calls_per_step": ncalls, "l2": "rotating %d weight copies (%.0f MB)" % (
+                           COPIES, COPIES * sum(weight_bytes(N, K, qt) for _, N, K, qt in LAYER) / 1e6),
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": per_step_launches * args.steps,
+            "clocks": clocks, "per_m": per_m, "peaks": peaks,
+        }
+        print(json.dumps(line))
+    if pg:
+        pg.destroy_process_group()
+
+
+def run_e2e(args, qmm, torch, dev, calls, wq, ws):
+    """The headline metric end to end through the public API with host buffers: the step's M <= 16 calls,
+    each copying its activations from pinned host memory to the device and its result back to pinned host
+    memory inside the timed region (weights stay resident, as a model's would)."""
+    stream = torch.cuda.current_stream()
+    small = [c for c in calls if c[4] <= 16]
+    hx, hy, dx, dy = {}, {}, {}, {}
+    for name, N, K, qt, M, b in small:
+        if (M, K) not in hx:
+            hx[(M, K)] = torch.from_numpy(synthetic.activations(M, K, seed=M)).pin_memory()
+            dx[(M, K)] = torch.empty((M, K), dtype=torch.float32, device=dev)
+        if (M, N) not in hy:
+            hy[(M, N)] = torch.empty((M, N), dtype=torch.float32).pin_memory()
+            dy[(M, N)] = torch.empty((M, N), dtype=torch.float32, device=dev)
+
+    def step(s):
+        for name, N, K, qt, M, b in small:
+            x, y = dx[(M, K)], dy[(M, N)]
+            x.copy_(hx[(M, K)], non_blocking=True)
+            qmm.qmm_ws(wq[(s % COPIES, name)], qt, N, K, x, y, ws)
+            hy[(M, N)].copy_(y, non_blocking=True)
+
+    steps = max(10, args.steps)
+    for s in range(3):
+        step(s)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(steps):
+        step(s)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    wb = sum(weight_bytes(c[1], c[2], c[3]) for c in small)
+    return {"value": round(wb / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": sum(c[4] * c[2] * 4 for c in small),
+            "d2h_bytes_per_step": sum(c[4] * c[1] * 4 for c in small), "steps": steps,
+            "calls": "the 21 calls with M<=16"}
+
+
+# ---------------------------------------------------------------------------------------- oracle legs
+
+def oracle_step_sample():
+    """The bounded sample the oracle times: the seven projections at M = 1, 2 and 7 (every M <= 16 call of
+    the step), on oracle-encoded copies of the same seeded weights."""
+    import oracle
+    ws = {}
+    for name, N, K, qt in LAYER:
+        ws[name] = oracle.quantize(qt, synthetic.weights(N, K, seed=0))
+    xs = {(M, K): synthetic.activations(M, K, seed=M) for M in (1, 2, 7) for K in {c[2] for c in LAYER}}
+    return oracle, ws, xs
+
+
+def time_oracle_sample(oracle, ws, xs):
+    t0 = time.perf_counter()
+    wb = 0.0
+    for M in (1, 2, 7):
+        for name, N, K, qt in LAYER:
+            oracle.qmm(qt, ws[name], N, K, xs[(M, K)])
+            wb += weight_bytes(N, K, qt)
+    return wb, time.perf_counter() - t0
+
+
+def cpu_baseline(args):
+    oracle, ws, xs = oracle_step_sample()
+    wb, t = time_oracle_sample(oracle, ws, xs)
+    return {"value": round(wb / t / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "the 21 calls with M<=16 (7 projections x M in {1,2,7}), full outputs, one pass (%.1f s)" % t}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    oracle, ws, xs = oracle_step_sample()
+    for _ in range(args.warmup):
+        time_oracle_sample(oracle, ws, xs)
+    t0 = time.perf_counter()
+    wb = 0.0
+    for _ in range(args.steps):
+        b, _t = time_oracle_sample(oracle, ws, xs)
+        wb += b
+    t = time.perf_counter() - t0
+    v = wb / t / 1e9
+    cores = oracle.num_threads()
+    sample = "per step: the 21 calls with M<=16 of the layer (7 projections x M in {1,2,7}), full outputs"
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--case", default=None, help="time one call only, e.g. ffn_gate:2048")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -190,11 +190,8 @@ def run_ours(args):
     import ctypes
     P = ctypes.c_void_p
 
-    def launches_of(M, K):
-        return 1 if qmm.qmm_pick_path("Q4_K", 1, K, M) == 0 else 2
-
     ncalls = len(calls)
-    per_step_launches = sum(launches_of(c[4], c[2]) for c in calls)
+    per_step_launches = sum(qmm.qmm_launch_count(c[3], c[1], c[2], c[4]) for c in calls)
 
     # raw argument tuples (C-ABI calls, no Python tensor work inside the timed loop)
     raw = []
@@ -283,6 +280,12 @@ def run_ours(args):
         d["us"] = round(d["us"], 2)
         del d["wbytes"], d["flops"]
 
+    if args.detail:
+        for i, c in enumerate(calls):
+            wb = weight_bytes(c[1], c[2], c[3])
+            print("%-12s M=%-5d b=%d %9.2f us %8.1f GB/s %8.2f TFLOP/s" % (
+                c[0], c[4], c[5], call_ms[i] * 1e3, wb / (call_ms[i] * 1e-3) / 1e9,
+                2.0 * c[4] * c[1] * c[2] / (call_ms[i] * 1e-3) / 1e12), file=sys.stderr)
     e2e = run_e2e(args, qmm, torch, dev, calls, wq, ws) if not args.case else None
     cpu = cpu_baseline(args) if (rank == 0 and world == 1 and not args.no_cpu and not args.case) else None
 
@@ -412,6 +415,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--case", default=None, help="time one call only, e.g. ffn_gate:2048")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    ap.add_argument("--detail", action="store_true", help="per-call device times on stderr")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

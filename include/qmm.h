@@ -80,9 +80,11 @@ enum qmm_type {
  * the tcgen05 tensor-core path with a 32/64/128-token tile picked by qmm_pick_tile(M). The tensor-core
  * path rounds x and the dequantized weights to bfloat16 (round to nearest even) and accumulates in
  * binary32; the mat-vec path multiplies the binary32 dequantized weights by x in binary32.
- * The tensor-core path with binary32 x needs M*K*2 bytes of scratch for the bfloat16 copy of x; qmm()
- * takes it from the stream-ordered allocator (cudaMallocAsync / cudaFreeAsync on `stream`). Callers
- * that manage memory themselves use qmm_ws().
+ * The tensor-core path needs device scratch: M*K*2 bytes for the bfloat16 copy of binary32 x, and, when
+ * few 128-row blocks leave most SMs idle and the K dimension is split over CTAs, S*M*N*4 bytes of binary32
+ * partial sums (added in a fixed order by a second kernel). qmm() takes the scratch from the stream-ordered
+ * allocator (cudaMallocAsync / cudaFreeAsync on `stream`); callers that manage memory themselves use
+ * qmm_ws() with qmm_workspace_size() bytes.
  */
 int qmm(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, float *y, void *stream);
 
@@ -127,6 +129,10 @@ int qmm_pick_tile(int64_t M);
 
 /* Which path qmm() takes for M tokens: 0 = mat-vec, 32/64/128 = tensor-core tile. */
 int qmm_pick_path(int qtype, int64_t N, int64_t K, int64_t M);
+
+/* How many kernels one qmm() / qmm_ws() call with these arguments launches (diagnostic; the mat-vec path
+ * may launch more when its activations have to be processed in smaller token groups). */
+int qmm_launch_count(int qtype, int64_t N, int64_t K, int64_t M);
 
 /*
  * qmm_dequant: w_out[n*K + k] = dequant(W)[n, k] as binary32. Each value is the exact value of the

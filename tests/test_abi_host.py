@@ -98,6 +98,19 @@ def test_pick_path(L):
 
 
 def test_workspace_size(L):
+    # the mat-vec path needs no scratch
     assert qmm.qmm_workspace_size("Q4_K", 4096, 2560, 1) == 0
-    assert qmm.qmm_workspace_size("Q4_K", 4096, 2560, 100) >= 100 * 2560 * 2
-    assert qmm.qmm_workspace_size("Q4_K", 4096, 2560, 100, x_bf16=True) == 0
+    # tensor-core path: a bf16 copy of binary32 activations ...
+    assert qmm.qmm_workspace_size("Q4_K", 9728, 2560, 2048) >= 2048 * 2560 * 2
+    assert qmm.qmm_workspace_size("Q4_K", 9728, 2560, 2048, x_bf16=True) == 0
+    # ... plus binary32 partials when few row blocks make the K dimension split over CTAs
+    fp32 = qmm.qmm_workspace_size("Q4_K", 1024, 2560, 100)
+    bf16 = qmm.qmm_workspace_size("Q4_K", 1024, 2560, 100, x_bf16=True)
+    assert bf16 >= 2 * 100 * 1024 * 4 and fp32 >= bf16 + 100 * 2560 * 2
+
+
+def test_launch_count(L):
+    assert qmm.qmm_launch_count("Q4_K", 9728, 2560, 1) == 1
+    assert qmm.qmm_launch_count("Q4_K", 9728, 2560, 2048) == 2            # bf16 copy of x + mm
+    assert qmm.qmm_launch_count("Q4_K", 9728, 2560, 2048, x_bf16=True) == 1
+    assert qmm.qmm_launch_count("Q4_K", 1024, 2560, 100) == 3             # + split-K reduction

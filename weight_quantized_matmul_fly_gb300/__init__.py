@@ -12,6 +12,7 @@ import ctypes
 import os
 
 __all__ = ["QmmError", "TYPES", "TYPE_ID", "X_BF16", "build", "lib", "qmm", "qmm_ws", "qmm_workspace_size",
+           "qmm_launch_count",
            "qmm_id", "qmm_with_tile", "qmm_pick_tile", "qmm_pick_path", "qmm_dequant", "qmm_quantize",
            "qmm_type_info", "qmm_get_status", "qmm_strerror", "row_bytes", "EXPORTS"]
 
@@ -26,7 +27,7 @@ STATUS_BAD_ID, STATUS_TIMEOUT = 0x1, 0x2
 
 # Every symbol include/qmm.h declares.
 EXPORTS = ["qmm", "qmm_ws", "qmm_workspace_size", "qmm_id", "qmm_with_tile", "qmm_pick_tile", "qmm_pick_path",
-           "qmm_dequant", "qmm_quantize", "qmm_type_info", "qmm_get_status", "qmm_strerror"]
+           "qmm_launch_count", "qmm_dequant", "qmm_quantize", "qmm_type_info", "qmm_get_status", "qmm_strerror"]
 
 
 class QmmError(RuntimeError):
@@ -59,6 +60,7 @@ def lib():
             "qmm_with_tile": ([P, I, I64, I64, P, I64, P, I, P], I),
             "qmm_pick_tile": ([I64], I),
             "qmm_pick_path": ([I, I64, I64, I64], I),
+            "qmm_launch_count": ([I, I64, I64, I64], I),
             "qmm_dequant": ([P, I, I64, I64, P, P], I),
             "qmm_quantize": ([P, I, I64, I64, P, P], I),
             "qmm_type_info": ([I, ctypes.POINTER(I), ctypes.POINTER(I)], I),
@@ -123,6 +125,10 @@ def qmm_pick_tile(M: int) -> int:
 
 def qmm_pick_path(qtype, N: int, K: int, M: int) -> int:
     return lib().qmm_pick_path(_qt(qtype), int(N), int(K), int(M))
+
+
+def qmm_launch_count(qtype, N: int, K: int, M: int, x_bf16: bool = False) -> int:
+    return lib().qmm_launch_count(_qt(qtype) | (X_BF16 if x_bf16 else 0), int(N), int(K), int(M))
 
 
 def qmm_workspace_size(qtype, N: int, K: int, M: int, x_bf16: bool = False) -> int:

@@ -218,7 +218,7 @@ __device__ void encode_block(const float *w, uint8_t *b) {
 }
 
 // One thread per block: the block's weights are copied to a local array, encoded into a local byte
-// buffer, then written out byte by byte (block starts are only 2-byte aligned in general).
+// buffer, then written out as 16-bit words (every block size is even and every block 2-byte aligned).
 template <int QT>
 __global__ void quantize_kernel(const float *__restrict__ w, int64_t N, int64_t K, uint8_t *__restrict__ out) {
     constexpr int QK = TypeInfo<QT>::QK, BYTES = TypeInfo<QT>::BYTES;
@@ -231,8 +231,19 @@ __global__ void quantize_kernel(const float *__restrict__ w, int64_t N, int64_t 
         for (int i = 0; i < QK; ++i) wl[i] = src[i];
         uint8_t bl[BYTES];
         encode_block<QT>(wl, bl);
-        uint8_t *dst = out + t * BYTES;
-        for (int i = 0; i < BYTES; ++i) dst[i] = bl[i];
+        uint16_t *dst = reinterpret_cast<uint16_t *>(out + t * BYTES);
+        for (int i = 0; i < BYTES / 2; ++i) dst[i] = (uint16_t)(bl[2 * i] | ((uint32_t)bl[2 * i + 1] << 8));
+    }
+}
+
+// Plain types: one element per thread, stored in the output's own width.
+template <int QT>
+__global__ void quantize_plain_kernel(const float *__restrict__ w, int64_t n, uint8_t *__restrict__ out) {
+    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
+        const float v = w[t];
+        if constexpr (QT == T_F32) reinterpret_cast<uint32_t *>(out)[t] = __float_as_uint(v);
+        else if constexpr (QT == T_F16) reinterpret_cast<uint16_t *>(out)[t] = (uint16_t)f16_bits(v);
+        else reinterpret_cast<uint16_t *>(out)[t] = (uint16_t)bf16_bits(v);
     }
 }
 
@@ -265,7 +276,10 @@ struct QuantizeLaunch {
         int64_t blocks = (total + threads - 1) / threads;
         if (blocks > 152 * 64) blocks = 152 * 64;
         if (blocks < 1) blocks = 1;
-        deq::quantize_kernel<QT><<<(unsigned)blocks, threads, 0, st>>>(w, N, K, static_cast<uint8_t *>(out));
+        if constexpr (QT <= T_BF16)
+            deq::quantize_plain_kernel<QT><<<(unsigned)blocks, threads, 0, st>>>(w, N * K, static_cast<uint8_t *>(out));
+        else
+            deq::quantize_kernel<QT><<<(unsigned)blocks, threads, 0, st>>>(w, N, K, static_cast<uint8_t *>(out));
         return cudaGetLastError() == cudaSuccess ? 0 : -6;
     }
 };

@@ -1,0 +1,734 @@
+// Tensor-core mat-vec path for small token counts (M <= 16) and quantized weight types.
+//
+// Why tensor cores here. At 4-6 bits per weight the HBM stream delivers about one weight per 2-3 CUDA-core
+// issue slots, so a binary32 FMA per weight per token cannot keep up beyond M = 1 or 2. The products are
+// instead run on mma.sync (m16n8k16, bf16 in, f32 accumulate) fed from registers:
+//   - A = the weights' integer codes (q - bias), which are exact in bf16 (|q| <= 32), 16 rows x 16 k;
+//   - B = the activations, 8 columns: for binary32 x each token takes two columns, x_hi = bf16(x) and
+//     x_lo = bf16(x - x_hi), so the product keeps ~17 bits of x (residual <= 2^-18 |x|) and the result
+//     stays in the binary32 tolerance class; bf16 x is exact and takes one column per token;
+//   - each scale unit's sum (16, 32 or 64 weights, which never straddle a k16 group) is scaled in binary32
+//     on the CUDA cores: y += ds * sum_k q x + off * sum_k x, with off the type's minimum or bias term.
+// tcgen05 is not used on this path: its A operand must come from shared or tensor memory, and writing the
+// decoded bf16 codes there costs 4 bytes of on-chip traffic per weight against the 0.56 bytes the weight
+// costs in HBM; mma.sync takes A straight from the registers the decoder wrote.
+//
+// Lane mapping. Lane (g, t) = (lane / 4, lane % 4) of a warp decodes rows g and g + 8 of the warp's 16-row
+// group, weights 4t .. 4t+3 of every 16-weight group, which mma.sync sees as logical k {2t, 2t+1, 2t+8,
+// 2t+9} (the activations are read with the same permutation). Every lane is busy at any K, which is what
+// the pages' narrow-K row split was for (llama.cpp PR 28086, "metal : fix idle threads in mul_mv_iq3_xxs
+// for ne00 < 1024", section "Overview"); and tokens are MMA columns, so the kernel is specialised on the
+// number of 4- or 8-token column groups (tiny-llm PR 122, "perf: Optimize quantized matmul for small
+// decode batches": the x_size buckets become column-group buckets).
+//
+// Work split. A CTA owns 16 rows per warp and one K segment; the K segments of a row block form a thread
+// block cluster, whose CTAs add their partial sums through distributed shared memory in a fixed order
+// (so the result is deterministic and no global scratch is needed).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "qmm_common.cuh"
+
+namespace wqk {
+namespace gtc {
+
+// ------------------------------------------------------------------------------------------ helpers
+__device__ __forceinline__ uint32_t ldw_a2(const uint8_t *p) { return ld_u16(p) | (ld_u16(p + 2) << 16); }
+
+// bf16x2 (lo, hi) of codes byte0/byte1 (lo pair) or byte2/byte3 (hi pair) minus `bias2` (bf16x2 of 128+bias).
+__device__ __forceinline__ uint32_t codes_pair(uint32_t codes, uint32_t sel, uint32_t bias2) {
+    const uint32_t m = __byte_perm(codes, 0x43434343u, sel);   // 128 + code, exact
+    __nv_bfloat162 v = __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&m),
+                               *reinterpret_cast<const __nv_bfloat162 *>(&bias2));
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+constexpr uint32_t SEL_LO = 0x5140u, SEL_HI = 0x7362u;
+__host__ __device__ constexpr uint32_t bias_bf16x2(int bias) {
+    // bf16 of 128 + bias for bias in [0, 32]: exponent 2^7, mantissa bias
+    return (uint32_t)(0x4300u | (uint32_t)bias) * 0x10001u;
+}
+
+// Signed int8 codes (Q8_0) -> two bf16x2 via binary32 (exact: |q| <= 128).
+__device__ __forceinline__ void codes_i8(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const float f0 = (float)(int8_t)(w & 255u), f1 = (float)(int8_t)((w >> 8) & 255u);
+    const float f2 = (float)(int8_t)((w >> 16) & 255u), f3 = (float)(int8_t)(w >> 24);
+    __nv_bfloat162 a = __floats2bfloat162_rn(f0, f1), b = __floats2bfloat162_rn(f2, f3);
+    lo = *reinterpret_cast<uint32_t *>(&a);
+    hi = *reinterpret_cast<uint32_t *>(&b);
+}
+
+// Spread 4 bits into bit `pos` of each byte.
+__device__ __forceinline__ uint32_t spread4(uint32_t b, int pos) {
+    return (((b & 1u)) | ((b & 2u) << 7) | ((b & 4u) << 14) | ((b & 8u) << 21)) << pos;
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                               const float (&c)[4]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+          "f"(c[3]));
+}
+
+// ------------------------------------------------------------------------------------------ per-type fragments
+// A macro block is 256 consecutive weights of a row (one K-quant super-block, 8 legacy blocks, 4 A4G64
+// blocks), 16 groups of 16 weights. For group u, lane t supplies 4 weights of each of its two rows;
+// Frag<QT> fixes which:
+//   load(r, mb, t, nblk)  reads what lane t needs of one macro block of one row (nblk valid blocks, for
+//                         the legacy types at a K tail);
+//   codes(r, u)           the lane's 4 stored codes of group u, one per byte;
+//   xoff(u, t)            offset, within the macro block, of the 4 consecutive weights those codes are
+//                         (the activations are read from the same place);
+//   UNIT                  weights per scale unit; the groups of unit s are u = s*UNIT/16 .. consecutive;
+//   scale(r, s, ds, off)  the unit's scale and additive term (w = ds*(q - BIAS) + off).
+// Types whose scales take several operations to unpack (the K-quants) set SPLIT: each lane then unpacks
+// only a quarter of the units and the others fetch them with a warp shuffle.
+template <int QT> struct Frag;
+
+__device__ __forceinline__ float small_u2f(uint32_t v) {   // exact for v < 2^23
+    return __int_as_float(0x4B000000 | v) - 8388608.0f;
+}
+__device__ __forceinline__ float small_i2f(int v) {         // exact for |v| < 2^22
+    return __int_as_float(0x4B400000 + v) - 12582912.0f;
+}
+
+template <> struct Frag<T_Q4_0> {
+    static constexpr int UNIT = 32, BIAS = 8;
+    static constexpr bool SPLIT = false;
+    struct Raw { uint32_t q[8]; float d[8]; };
+    __device__ static void load(Raw &r, const uint8_t *mb, int t, int nblk) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            if (b < nblk) {
+                r.q[b] = ldw_a2(mb + 18 * b + 2 + 4 * t);
+                r.d[b] = h2f(ld_u16(mb + 18 * b));
+            } else { r.q[b] = 0; r.d[b] = 0.0f; }
+        }
+    }
+    __device__ static uint32_t codes(const Raw &r, int u) { return (r.q[u >> 1] >> (4 * (u & 1))) & 0x0F0F0F0Fu; }
+    __device__ static int xoff(int u, int t) { return 16 * u + 4 * t; }
+    __device__ static void scale(const Raw &r, int s, float &ds, float &off) { ds = r.d[s]; off = 0.0f; }
+};
+
+template <> struct Frag<T_Q4_1> {
+    static constexpr int UNIT = 32, BIAS = 0;
+    static constexpr bool SPLIT = false;
+    struct Raw { uint32_t q[8]; uint32_t dm[8]; };
+    __device__ static void load(Raw &r, const uint8_t *mb, int t, int nblk) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            if (b < nblk) {
+                r.q[b] = ld_u32(mb + 20 * b + 4 + 4 * t);
+                r.dm[b] = ld_u32(mb + 20 * b);
+            } else { r.q[b] = 0; r.dm[b] = 0; }
+        }
+    }
+    __device__ static uint32_t codes(const Raw &r, int u) { return (r.q[u >> 1] >> (4 * (u & 1))) & 0x0F0F0F0Fu; }
+    __device__ static int xoff(int u, int t) { return 16 * u + 4 * t; }
+    __device__ static void scale(const Raw &r, int s, float &ds, float &off) {
+        ds = h2f(r.dm[s] & 0xffffu); off = h2f(r.dm[s] >> 16);
+    }
+};
+
+// Q5_0 / Q5_1: element 16h + 4t + j of a block is the low (h = 0) or high (h = 1) nibble of qs[4t + j]
+// plus bit 16h + 4t + j of qh as the fifth bit.
+template <int QT> struct FragQ5 {
+    static constexpr bool ONE = QT == T_Q5_1;
+    static constexpr int UNIT = 32, BIAS = ONE ? 0 : 16, BYTES = ONE ? 24 : 22, QS = ONE ? 8 : 6, QH = ONE ? 4 : 2;
+    static constexpr bool SPLIT = false;
+    struct Raw { uint32_t q[8]; uint32_t qh[8]; uint32_t dm[8]; };
+    __device__ static void load(Raw &r, const uint8_t *mb, int t, int nblk) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            if (b < nblk) {
+                r.q[b] = ONE ? ld_u32(mb + BYTES * b + QS + 4 * t) : ldw_a2(mb + BYTES * b + QS + 4 * t);
+                r.qh[b] = ((ONE ? ld_u32(mb + BYTES * b + QH) : ldw_a2(mb + BYTES * b + QH)) >> (4 * t)) & 0x000F000Fu;
+                r.dm[b] = ONE ? ld_u32(mb + BYTES * b) : ld_u16(mb + BYTES * b);
+            } else { r.q[b] = 0; r.qh[b] = 0; r.dm[b] = 0; }
+        }
+    }
+    __device__ static uint32_t codes(const Raw &r, int u) {
+        const int b = u >> 1, h = u & 1;
+        return ((r.q[b] >> (4 * h)) & 0x0F0F0F0Fu) | spread4((r.qh[b] >> (16 * h)) & 15u, 4);
+    }
+    __device__ static int xoff(int u, int t) { return 16 * u + 4 * t; }
+    __device__ static void scale(const Raw &r, int s, float &ds, float &off) {
+        ds = h2f(r.dm[s] & 0xffffu);
+        off = ONE ? h2f(r.dm[s] >> 16) : 0.0f;
+    }
+};
+template <> struct Frag<T_Q5_0> : FragQ5<T_Q5_0> {};
+template <> struct Frag<T_Q5_1> : FragQ5<T_Q5_1> {};
+
+template <> struct Frag<T_Q8_0> {
+    static constexpr int UNIT = 32, BIAS = 0;
+    static constexpr bool SPLIT = false;
+    struct Raw { uint32_t q[16]; float d[8]; };
+    __device__ static void load(Raw &r, const uint8_t *mb, int t, int nblk) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            if (b < nblk) {
+                r.q[2 * b] = ldw_a2(mb + 34 * b + 2 + 4 * t);
+                r.q[2 * b + 1] = ldw_a2(mb + 34 * b + 18 + 4 * t);
+                r.d[b] = h2f(ld_u16(mb + 34 * b));
+            } else { r.q[2 * b] = 0; r.q[2 * b + 1] = 0; r.d[b] = 0.0f; }
+        }
+    }
+    __device__ static int xoff(int u, int t) { return 16 * u + 4 * t; }
+    __device__ static void scale(const Raw &r, int s, float &ds, float &off) { ds = r.d[s]; off = 0.0f; }
+};
+
+template <> struct Frag<T_Q2_K> {
+    static constexpr int UNIT = 16, BIAS = 0;
+    static constexpr bool SPLIT = true;
+    struct Raw { uint32_t q[4]; uint32_t sc; uint32_t dd; };
+    // lane t keeps the sub-block scale bytes of units 4t .. 4t+3 (scales[4t .. 4t+3])
+    __device__ static void load(Raw &r, const uint8_t *mb, int t, int) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) r.q[i] = ld_u32(mb + 16 + 32 * (i >> 1) + 16 * (i & 1) + 4 * t);
+        r.sc = ld_u32(mb + 4 * t);
+        r.dd = ld_u32(mb + 80);
+    }
+    __device__ static uint32_t codes(const Raw &r, int u) {
+        return (r.q[2 * (u >> 3) + (u & 1)] >> (2 * ((u & 7) >> 1))) & 0x03030303u;
+    }
+    __device__ static int xoff(int u, int t) { return 16 * u + 4 * t; }
+    // unit 4t + i of this lane
+    __device__ static void scale_own(const Raw &r, int i, float &ds, float &off) {
+        const uint32_t b = (r.sc >> (8 * i)) & 255u;
+        ds = __fmul_rn(h2f(r.dd & 0xffffu), small_u2f(b & 15u));
+        off = -__fmul_rn(h2f(r.dd >> 16), small_u2f(b >> 4));
+    }
+};
+
+template <> struct Frag<T_Q3_K> {
+    static constexpr int UNIT = 16, BIAS = 4;
+    static constexpr bool SPLIT = true;
+    struct Raw { uint32_t q[4]; uint32_t hm[2]; uint32_t s[3]; float d; };
+    __device__ static void load(Raw &r, const uint8_t *mb, int t, int) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) r.q[i] = ldw_a2(mb + 32 + 32 * (i >> 1) + 16 * (i & 1) + 4 * t);
+        r.hm[0] = ldw_a2(mb + 4 * t);
+        r.hm[1] = ldw_a2(mb + 16 + 4 * t);
+#pragma unroll
+        for (int i = 0; i < 3; ++i) r.s[i] = ldw_a2(mb + 96 + 4 * i);
+        r.d = h2f(ld_u16(mb + 108));
+    }
+    __device__ static uint32_t codes(const Raw &r, int u) {
+        const uint32_t lo = (r.q[2 * (u >> 3) + (u & 1)] >> (2 * ((u & 7) >> 1))) & 0x03030303u;
+        const uint32_t hb = (r.hm[u & 1] >> (u >> 1)) & 0x01010101u;
+        return lo | (hb << 2);
+    }
+    __device__ static int xoff(int u, int t) { return 16 * u + 4 * t; }
+    __device__ static void scale_own_t(const Raw &r, int s, float &ds, float &off) {
+        ds = __fmul_rn(r.d, small_i2f((int)six_bits(r.s[0], r.s[1], r.s[2], s) - 32));
+        off = 0.0f;
+    }
+};
+
+// Q4_K / Q5_K: lane t reads 8 consecutive code bytes of each 32-byte chunk c of qs, which hold weights
+// 8t .. 8t+7 of sub-blocks 2c (low nibbles) and 2c+1 (high nibbles). Group u = 4c + 2*nib + hb takes the
+// low (hb = 0) or high (hb = 1) four of them, nib selecting the sub-block.
+template <int QT> struct FragQ45K {
+    static constexpr int UNIT = 32, BIAS = 0;
+    static constexpr bool SPLIT = true;
+    struct Raw { uint2 q[4]; uint2 qh; uint32_t s0, s1, s2; uint32_t dd; };
+    __device__ static void load(Raw &r, const uint8_t *mb, int t, int) {
+        const uint4 hd = ld_u128(mb);
+        r.dd = hd.x; r.s0 = hd.y; r.s1 = hd.z; r.s2 = hd.w;
+        constexpr int QOFF = QT == T_Q4_K ? 16 : 48;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) r.q[c] = *reinterpret_cast<const uint2 *>(mb + QOFF + 32 * c + 8 * t);
+        if (QT == T_Q5_K) r.qh = *reinterpret_cast<const uint2 *>(mb + 16 + 8 * t);
+    }
+    __device__ static uint32_t codes(const Raw &r, int u) {
+        const int c = u >> 2, nib = (u >> 1) & 1, hb = u & 1;
+        const uint32_t w = hb ? r.q[c].y : r.q[c].x;
+        uint32_t v = (w >> (4 * nib)) & 0x0F0F0F0Fu;
+        if (QT == T_Q5_K) v |= (((hb ? r.qh.y : r.qh.x) >> (u >> 1)) & 0x01010101u) << 4;
+        return v;
+    }
+    __device__ static int xoff(int u, int t) { return 32 * (u >> 1) + 8 * t + 4 * (u & 1); }
+    __device__ static void scale_own_t(const Raw &r, int s, float &ds, float &off) {
+        ds = __fmul_rn(h2f(r.dd & 0xffffu), small_u2f(six_bits(r.s0, r.s1, r.s2, s)));
+        off = -__fmul_rn(h2f(r.dd >> 16), small_u2f(six_bits(r.s0, r.s1, r.s2, 8 + s)));
+    }
+};
+template <> struct Frag<T_Q4_K> : FragQ45K<T_Q4_K> {};
+template <> struct Frag<T_Q5_K> : FragQ45K<T_Q5_K> {};
+
+template <> struct Frag<T_Q6_K> {
+    static constexpr int UNIT = 16, BIAS = 32;
+    static constexpr bool SPLIT = true;
+    struct Raw { uint32_t ql[8]; uint32_t qh[4]; uint32_t sc; float d; };
+    // lane t keeps the int8 scales of units 4t .. 4t+3. The block starts 4-byte aligned or 2 past it.
+    __device__ static void load(Raw &r, const uint8_t *mb, int t, int) {
+        if ((reinterpret_cast<uintptr_t>(mb) & 3u) == 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) r.ql[i] = ld_u32(mb + 64 * (i >> 2) + 16 * (i & 3) + 4 * t);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) r.qh[i] = ld_u32(mb + 128 + 32 * (i >> 1) + 16 * (i & 1) + 4 * t);
+            r.sc = ld_u32(mb + 192 + 4 * t);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) r.ql[i] = ldw_a2(mb + 64 * (i >> 2) + 16 * (i & 3) + 4 * t);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) r.qh[i] = ldw_a2(mb + 128 + 32 * (i >> 1) + 16 * (i & 1) + 4 * t);
+            r.sc = ldw_a2(mb + 192 + 4 * t);
+        }
+        r.d = h2f(ld_u16(mb + 208));
+    }
+    __device__ static uint32_t codes(const Raw &r, int u) {
+        const int h = u >> 3;
+        const uint32_t lo = (r.ql[4 * h + (u & 3)] >> (4 * ((u & 7) >> 2))) & 0x0F0F0F0Fu;
+        const uint32_t hb = (r.qh[2 * h + (u & 1)] >> (2 * ((u & 7) >> 1))) & 0x03030303u;
+        return lo | (hb << 4);
+    }
+    __device__ static int xoff(int u, int t) { return 16 * u + 4 * t; }
+    __device__ static void scale_own(const Raw &r, int i, float &ds, float &off) {
+        ds = __fmul_rn(r.d, small_i2f((int)(int8_t)((r.sc >> (8 * i)) & 255u)));
+        off = 0.0f;
+    }
+};
+
+template <> struct Frag<T_A4G64> {
+    static constexpr int UNIT = 64, BIAS = 0;
+    static constexpr bool SPLIT = false;
+    struct Raw { uint32_t q[8]; uint32_t sb[4]; };
+    __device__ static void load(Raw &r, const uint8_t *mb, int t, int nblk) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            if (b < nblk) {
+                r.q[2 * b] = ld_u32(mb + 36 * b + 4 + 4 * t);
+                r.q[2 * b + 1] = ld_u32(mb + 36 * b + 20 + 4 * t);
+                r.sb[b] = ld_u32(mb + 36 * b);
+            } else { r.q[2 * b] = 0; r.q[2 * b + 1] = 0; r.sb[b] = 0; }
+        }
+    }
+    __device__ static uint32_t codes(const Raw &r, int u) {
+        return (r.q[2 * (u >> 2) + (u & 1)] >> (4 * ((u & 3) >> 1))) & 0x0F0F0F0Fu;
+    }
+    __device__ static int xoff(int u, int t) { return 16 * u + 4 * t; }
+    __device__ static void scale(const Raw &r, int s, float &ds, float &off) {
+        ds = bf2f(r.sb[s] & 0xffffu); off = bf2f(r.sb[s] >> 16);
+    }
+};
+
+// The scale units a lane unpacks itself when SPLIT: units [t*UPL, (t+1)*UPL), UPL = units per lane.
+template <int QT> struct OwnScales {
+    static constexpr int UPL = (256 / Frag<QT>::UNIT) / 4;
+    float ds[UPL], off[UPL];
+};
+template <int QT>
+__device__ __forceinline__ void own_scales(const typename Frag<QT>::Raw &r, int t, OwnScales<QT> &o) {
+    constexpr int UPL = OwnScales<QT>::UPL;
+#pragma unroll
+    for (int i = 0; i < UPL; ++i) {
+        if constexpr (QT == T_Q2_K || QT == T_Q6_K) Frag<QT>::scale_own(r, i, o.ds[i], o.off[i]);
+        else Frag<QT>::scale_own_t(r, UPL * t + i, o.ds[i], o.off[i]);
+    }
+}
+// (ds, off) of unit s (compile-time) for the row this lane's group g decodes: from lane (g, s / UPL).
+template <int QT>
+__device__ __forceinline__ void unit_scale(const typename Frag<QT>::Raw &r, const OwnScales<QT> &o, int s, int g,
+                                           float &ds, float &off) {
+    if constexpr (Frag<QT>::SPLIT) {
+        constexpr int UPL = OwnScales<QT>::UPL;
+        const int src = 4 * g + s / UPL;
+        ds = __shfl_sync(0xffffffffu, o.ds[s % UPL], src);
+        off = (QT == T_Q6_K || QT == T_Q3_K) ? 0.0f : __shfl_sync(0xffffffffu, o.off[s % UPL], src);
+    } else {
+        Frag<QT>::scale(r, s, ds, off);
+    }
+}
+
+// A operand halves (lo pair, hi pair) of one row for 16-weight group u.
+template <int QT>
+__device__ __forceinline__ void frag_codes(const typename Frag<QT>::Raw &r, int u, uint32_t &lo, uint32_t &hi) {
+    if constexpr (QT == T_Q8_0) {
+        codes_i8(r.q[u], lo, hi);
+    } else {
+        const uint32_t c = Frag<QT>::codes(r, u);
+        constexpr uint32_t B2 = bias_bf16x2(Frag<QT>::BIAS);
+        lo = codes_pair(c, SEL_LO, B2);
+        hi = codes_pair(c, SEL_HI, B2);
+    }
+}
+
+// ------------------------------------------------------------------------------------------ the kernel
+// Shared memory: activations of the CTA's K segment as bf16 columns (xs), per-unit activation sums (sx)
+// and the partial results that the warps of a CTA, then the CTAs of a cluster, add up (part).
+template <int NT, bool XBF16> struct Layout {
+    static constexpr int COLS = 8 * NT;              // MMA columns
+    static constexpr int TOK = XBF16 ? 8 * NT : 4 * NT;   // tokens served
+    static constexpr int WARPS = 8;
+    __host__ __device__ static int xs_stride(int kpad) { return kpad + 16; }   // elements; +32 B breaks bank aliasing
+    __host__ __device__ static size_t bytes(int kpad, int unit) {
+        return (size_t)COLS * xs_stride(kpad) * 2 + (size_t)TOK * (kpad / unit) * 4 + (size_t)WARPS * 16 * TOK * 4;
+    }
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_dsmem_f32(const float *local, uint32_t rank) {
+    uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local)), ra;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+    return v;
+}
+
+// One macro block of two rows into the accumulators. FULL: all 16 groups lie inside K.
+template <int QT, int NT, bool XBF16, bool FULL>
+__device__ __forceinline__ void macro_step(const typename Frag<QT>::Raw &cur0, const typename Frag<QT>::Raw &cur1,
+                                           const __nv_bfloat16 *xs, int xst, const float *sx, int sxs, int kloc,
+                                           int nvalid, int g, int t, float (&acc)[NT][4]) {
+    using F = Frag<QT>;
+    constexpr int UNIT = F::UNIT, GPU = UNIT / 16;
+    // types without an additive term (w = ds * (q - bias))
+    constexpr bool SYM = QT == T_Q4_0 || QT == T_Q5_0 || QT == T_Q8_0 || QT == T_Q3_K || QT == T_Q6_K;
+    OwnScales<QT> own0, own1;
+    if constexpr (F::SPLIT) {
+        own_scales<QT>(cur0, t, own0);
+        own_scales<QT>(cur1, t, own1);
+    }
+    float d[NT][4];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+        if (!FULL && u >= nvalid) break;
+        uint32_t a[4];
+        frag_codes<QT>(cur0, u, a[0], a[2]);
+        frag_codes<QT>(cur1, u, a[1], a[3]);
+        const int xo = kloc + F::xoff(u, t);
+#pragma unroll
+        for (int mt = 0; mt < NT; ++mt) {
+            const uint2 b = *reinterpret_cast<const uint2 *>(xs + (size_t)(8 * mt + g) * xst + xo);
+            if ((u % GPU) == 0) {
+                const float z[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_bf16_16816(d[mt], a, b.x, b.y, z);
+            } else {
+                mma_bf16_16816(d[mt], a, b.x, b.y, d[mt]);
+            }
+        }
+        if ((u % GPU) == GPU - 1) {
+            const int su = u / GPU;                      // scale unit within the macro block
+            const int sul = (kloc + 16 * u) / UNIT;      // scale unit within the segment
+            float ds0, of0, ds1, of1;
+            unit_scale<QT>(cur0, own0, su, g, ds0, of0);
+            unit_scale<QT>(cur1, own1, su, g, ds1, of1);
+#pragma unroll
+            for (int mt = 0; mt < NT; ++mt) {
+                if constexpr (XBF16 && SYM) {
+                    acc[mt][0] = fmaf(ds0, d[mt][0], acc[mt][0]);
+                    acc[mt][1] = fmaf(ds0, d[mt][1], acc[mt][1]);
+                    acc[mt][2] = fmaf(ds1, d[mt][2], acc[mt][2]);
+                    acc[mt][3] = fmaf(ds1, d[mt][3], acc[mt][3]);
+                } else if constexpr (XBF16) {
+                    const int tk = 8 * mt + 2 * t;
+                    const float sx0 = sx[tk * sxs + sul], sx1 = sx[(tk + 1) * sxs + sul];
+                    acc[mt][0] = fmaf(ds0, d[mt][0], fmaf(of0, sx0, acc[mt][0]));
+                    acc[mt][1] = fmaf(ds0, d[mt][1], fmaf(of0, sx1, acc[mt][1]));
+                    acc[mt][2] = fmaf(ds1, d[mt][2], fmaf(of1, sx0, acc[mt][2]));
+                    acc[mt][3] = fmaf(ds1, d[mt][3], fmaf(of1, sx1, acc[mt][3]));
+                } else if constexpr (SYM) {
+                    acc[mt][0] = fmaf(ds0, d[mt][0] + d[mt][1], acc[mt][0]);
+                    acc[mt][2] = fmaf(ds1, d[mt][2] + d[mt][3], acc[mt][2]);
+                } else {
+                    const float sxt = sx[(4 * mt + t) * sxs + sul];
+                    acc[mt][0] = fmaf(ds0, d[mt][0] + d[mt][1], fmaf(of0, sxt, acc[mt][0]));
+                    acc[mt][2] = fmaf(ds1, d[mt][2] + d[mt][3], fmaf(of1, sxt, acc[mt][2]));
+                }
+            }
+        }
+    }
+}
+
+// CTA: 8 warps = RG row groups of 16 rows x KW slices of the CTA's K segment; the cluster's S CTAs take
+// consecutive K segments of the same rows.
+template <int QT, int NT, bool XBF16, int KW>
+__global__ void __launch_bounds__(256, 2)
+    gemv_tc_kernel(const uint8_t *__restrict__ wq, int N, int64_t K, int64_t rowbytes, const void *__restrict__ x,
+                   int M, float *__restrict__ y, int kseg) {
+    using F = Frag<QT>;
+    using LY = Layout<NT, XBF16>;
+    constexpr int WARPS = LY::WARPS, RG = WARPS / KW;
+    constexpr int UNIT = F::UNIT;
+    constexpr int TOK = LY::TOK;
+    constexpr int QK = TypeInfo<QT>::QK, BYTES = TypeInfo<QT>::BYTES;
+    constexpr int BPM = 256 / QK;                     // blocks per macro block
+    extern __shared__ __align__(16) uint8_t smem[];
+
+    const int S = gridDim.y;
+    const int64_t kb = (int64_t)blockIdx.y * kseg;
+    const int64_t ke = (kb + kseg < K) ? kb + kseg : K;
+    const int kpad = kseg;                            // multiple of 256
+    const int xst = LY::xs_stride(kpad), sxs = kpad / UNIT;
+    __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(smem);
+    float *sx = reinterpret_cast<float *>(smem + (size_t)LY::COLS * xst * 2);
+    float *part = sx + (size_t)TOK * sxs;             // [WARPS][16][TOK]
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const int rg = warp / KW, ks = warp % KW;
+    const int nrow0 = blockIdx.x * (16 * RG) + 16 * rg;
+    const int r0 = nrow0 + g, r1 = nrow0 + g + 8;
+    const uint8_t *row0 = wq + (int64_t)(r0 < N ? r0 : N - 1) * rowbytes;
+    const uint8_t *row1 = wq + (int64_t)(r1 < N ? r1 : N - 1) * rowbytes;
+    // this warp's macro blocks: a balanced share of the segment's
+    const int64_t smb = kb / 256, nmb = (ke - kb + 255) / 256;
+    const int64_t mb_beg = smb + (nmb * ks) / KW, mb_end = smb + (nmb * (ks + 1)) / KW;
+    const int64_t nblocks_row = K / QK;
+    const int64_t full_end = K / 256;                 // macro blocks lying entirely inside K
+
+    // The weights are read before waiting for the preceding kernel in the stream (they are model data
+    // that no kernel of this library writes); activations and outputs only after.
+    typename F::Raw cur0, cur1, nxt0, nxt1;
+    auto nblk_of = [&](int64_t mb) {
+        const int64_t r = nblocks_row - mb * BPM;
+        return (int)(r < BPM ? r : BPM);
+    };
+    if (mb_beg < mb_end) {
+        F::load(cur0, row0 + mb_beg * BPM * BYTES, t, nblk_of(mb_beg));
+        F::load(cur1, row1 + mb_beg * BPM * BYTES, t, nblk_of(mb_beg));
+    }
+    asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // ---- stage this segment's activations (tokens < M): bf16 columns and per-unit sums
+    {
+        const int k4n = kpad / 4;
+        const int mtok = M < TOK ? M : TOK;
+        for (int idx = tid; idx < mtok * k4n; idx += WARPS * 32) {
+            const int tok = idx / k4n, k4 = idx - tok * k4n;
+            const int64_t k = kb + 4 * k4;
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            if (k < ke) {
+                if constexpr (XBF16) {
+                    const uint2 p = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(x) +
+                                                                          (int64_t)tok * K + k));
+                    v[0] = __uint_as_float(p.x << 16); v[1] = __uint_as_float(p.x & 0xffff0000u);
+                    v[2] = __uint_as_float(p.y << 16); v[3] = __uint_as_float(p.y & 0xffff0000u);
+                } else {
+                    const float4 p = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(x) +
+                                                                           (int64_t)tok * K + k));
+                    v[0] = p.x; v[1] = p.y; v[2] = p.z; v[3] = p.w;
+                }
+            }
+            if constexpr (XBF16) {
+                __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]), h1 = __floats2bfloat162_rn(v[2], v[3]);
+                *reinterpret_cast<uint2 *>(xs + (size_t)tok * xst + 4 * k4) =
+                    make_uint2(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1));
+            } else {
+                float hi[4], lo[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    hi[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
+                    lo[j] = __fsub_rn(v[j], hi[j]);
+                }
+                __nv_bfloat162 h0 = __floats2bfloat162_rn(hi[0], hi[1]), h1 = __floats2bfloat162_rn(hi[2], hi[3]);
+                __nv_bfloat162 l0 = __floats2bfloat162_rn(lo[0], lo[1]), l1 = __floats2bfloat162_rn(lo[2], lo[3]);
+                const int col = 8 * (tok >> 2) + 2 * (tok & 3);
+                *reinterpret_cast<uint2 *>(xs + (size_t)col * xst + 4 * k4) =
+                    make_uint2(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1));
+                *reinterpret_cast<uint2 *>(xs + (size_t)(col + 1) * xst + 4 * k4) =
+                    make_uint2(*reinterpret_cast<uint32_t *>(&l0), *reinterpret_cast<uint32_t *>(&l1));
+            }
+            // per-unit sums of x (binary32, original values), reduced over the UNIT/4 lanes of a unit
+            float s = (v[0] + v[1]) + (v[2] + v[3]);
+#pragma unroll
+            for (int off = 1; off < UNIT / 4; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+            if ((k4 & (UNIT / 4 - 1)) == 0) sx[tok * sxs + (4 * k4) / UNIT] = s;
+        }
+    }
+    __syncthreads();
+
+    float acc[NT][4];
+#pragma unroll
+    for (int mt = 0; mt < NT; ++mt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[mt][j] = 0.0f;
+
+    for (int64_t mb = mb_beg; mb < mb_end; ++mb) {
+        if (mb + 1 < mb_end) {
+            F::load(nxt0, row0 + (mb + 1) * BPM * BYTES, t, nblk_of(mb + 1));
+            F::load(nxt1, row1 + (mb + 1) * BPM * BYTES, t, nblk_of(mb + 1));
+        }
+        const int kloc = (int)(mb * 256 - kb);    // position of this macro block in the segment
+        if (mb < full_end) {
+            macro_step<QT, NT, XBF16, true>(cur0, cur1, xs, xst, sx, sxs, kloc, 16, g, t, acc);
+        } else {
+            macro_step<QT, NT, XBF16, false>(cur0, cur1, xs, xst, sx, sxs, kloc, (int)((K - mb * 256) / 16), g, t,
+                                             acc);
+        }
+        cur0 = nxt0;
+        cur1 = nxt1;
+    }
+
+    // ---- results. binary32 x: acc[mt][0] = (row g, token 4mt+t), acc[mt][2] = (row g+8, token 4mt+t);
+    //      bf16 x: acc[mt][0/1] = (row g, tokens 8mt+2t, +1), acc[mt][2/3] = (row g+8, same tokens).
+    float *pw = part + (size_t)warp * 16 * TOK;
+#pragma unroll
+    for (int mt = 0; mt < NT; ++mt) {
+        if constexpr (XBF16) {
+            const int tk = 8 * mt + 2 * t;
+            pw[g * TOK + tk] = acc[mt][0]; pw[g * TOK + tk + 1] = acc[mt][1];
+            pw[(g + 8) * TOK + tk] = acc[mt][2]; pw[(g + 8) * TOK + tk + 1] = acc[mt][3];
+        } else {
+            const int tk = 4 * mt + t;
+            pw[g * TOK + tk] = acc[mt][0];
+            pw[(g + 8) * TOK + tk] = acc[mt][2];
+        }
+    }
+    __syncthreads();
+    // add the KW slices (fixed order) into the first slice's partials
+    const int mtok = M < TOK ? M : TOK;
+    for (int idx = tid; idx < RG * 16 * mtok; idx += WARPS * 32) {
+        const int r = idx / mtok, tk = idx - r * mtok;     // r: row within the CTA
+        const int rgi = r >> 4, rr = r & 15;
+        float s = 0.0f;
+#pragma unroll
+        for (int q = 0; q < KW; ++q) s += part[((size_t)(rgi * KW + q) * 16 + rr) * TOK + tk];
+        if (S == 1) {
+            const int n = blockIdx.x * (16 * RG) + r;
+            if (n < N) y[(int64_t)tk * N + n] = s;
+        } else {
+            part[((size_t)(rgi * KW) * 16 + rr) * TOK + tk] = s;
+        }
+    }
+    if (S > 1) {
+        cluster_sync();
+        if (cluster_rank() == 0) {
+            for (int idx = tid; idx < RG * 16 * mtok; idx += WARPS * 32) {
+                const int r = idx / mtok, tk = idx - r * mtok;
+                const int rgi = r >> 4, rr = r & 15;
+                const float *src = &part[((size_t)(rgi * KW) * 16 + rr) * TOK + tk];
+                float s = 0.0f;
+                for (int q = 0; q < S; ++q) s += ld_dsmem_f32(src, (uint32_t)q);
+                const int n = blockIdx.x * (16 * RG) + r;
+                if (n < N) y[(int64_t)tk * N + n] = s;
+            }
+        }
+        cluster_sync();
+    }
+}
+
+}  // namespace gtc
+
+// ------------------------------------------------------------------------------------------ host side
+namespace {
+
+template <int QT, int NT, bool XBF16, int KW>
+int launch_gtc_kw(const void *wq, int64_t N, int64_t K, const void *x, int M, float *y, int64_t S, int64_t kseg,
+                  cudaStream_t st) {
+    using LY = gtc::Layout<NT, XBF16>;
+    constexpr int UNIT = gtc::Frag<QT>::UNIT, RG = LY::WARPS / KW;
+    auto kern = gtc::gemv_tc_kernel<QT, NT, XBF16, KW>;
+    static bool attr_set = false;   // once per kernel instance
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024) != cudaSuccess)
+            return -6;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((N + 16 * RG - 1) / (16 * RG)), (unsigned)S, 1);
+    cfg.blockDim = dim3(LY::WARPS * 32, 1, 1);
+    cfg.dynamicSmemBytes = LY::bytes((int)kseg, UNIT);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)S;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t *>(wq), (int)N, K, row_bytes(QT, K), x,
+                                       M, y, (int)kseg);
+    return e == cudaSuccess ? 0 : -6;
+}
+
+// Work split: row groups of 16 x K slices, aiming at about `target` warps in flight (a full wave of
+// 2 CTAs x 8 warps per SM), K slices of at least one macro block, at most 8 CTAs per cluster and a
+// shared-memory budget for the staged activations.
+template <int QT, int NT, bool XBF16>
+int launch_gtc_t(const void *wq, int64_t N, int64_t K, const void *x, int M, float *y, cudaStream_t st) {
+    using LY = gtc::Layout<NT, XBF16>;
+    constexpr int UNIT = gtc::Frag<QT>::UNIT;
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 148;
+    }
+    const int64_t target = (int64_t)sms * 16;
+    const int64_t ngroups = (N + 15) / 16;
+    const int64_t nmacro = (K + 255) / 256;
+    int64_t slices = (target + ngroups - 1) / ngroups;            // K slices wanted per row group
+    if (slices > nmacro) slices = nmacro;
+    if (slices > 64) slices = 64;
+    if (slices < 1) slices = 1;
+    // Each CTA stages its K segment of the activations, so the activation bytes a CTA reads grow with M
+    // while its weight bytes grow with its rows: larger M keeps more row groups (fewer K slices) per CTA.
+    const int kw_cap = M <= 2 ? 8 : (M <= 8 ? 2 : 1);
+    int kw = 1;
+    while (kw < kw_cap && kw * 2 <= slices) kw *= 2;
+    int64_t S = (slices + kw - 1) / kw;
+    if (S > 8) S = 8;
+    // shared-memory budget: the CTA stages its whole K segment of activations
+    int64_t kseg = ((nmacro + S - 1) / S) * 256;
+    while (LY::bytes((int)kseg, UNIT) > 100 * 1024) {
+        if (S >= 8) return -3;                                    // caller splits the tokens
+        ++S;
+        kseg = ((nmacro + S - 1) / S) * 256;
+    }
+    S = (K + kseg - 1) / kseg;
+    switch (kw) {
+    case 1: return launch_gtc_kw<QT, NT, XBF16, 1>(wq, N, K, x, M, y, S, kseg, st);
+    case 2: return launch_gtc_kw<QT, NT, XBF16, 2>(wq, N, K, x, M, y, S, kseg, st);
+    case 4: return launch_gtc_kw<QT, NT, XBF16, 4>(wq, N, K, x, M, y, S, kseg, st);
+    default: return launch_gtc_kw<QT, NT, XBF16, 8>(wq, N, K, x, M, y, S, kseg, st);
+    }
+}
+
+struct GtcLaunch {
+    bool xbf16;
+    const void *wq;
+    int64_t N, K;
+    const void *x;
+    int M;
+    float *y;
+    cudaStream_t st;
+    template <int QT> int operator()() {
+        if constexpr (QT <= T_BF16) {
+            return -1;
+        } else {
+            if (xbf16) return M <= 8 ? launch_gtc_t<QT, 1, true>(wq, N, K, x, M, y, st)
+                                     : launch_gtc_t<QT, 2, true>(wq, N, K, x, M, y, st);
+            if (M <= 4) return launch_gtc_t<QT, 1, false>(wq, N, K, x, M, y, st);
+            if (M <= 8) return launch_gtc_t<QT, 2, false>(wq, N, K, x, M, y, st);
+            return launch_gtc_t<QT, 4, false>(wq, N, K, x, M, y, st);
+        }
+    }
+};
+
+}  // namespace
+
+// M <= 16 tokens (bigger M is split into groups of 16 by the caller). Returns -3 when the K segments a
+// cluster allows cannot hold the activations of this many tokens (the caller then halves the group).
+int launch_gemv_tc(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int M, float *y,
+                   cudaStream_t st) {
+    GtcLaunch f{xbf16, wq, N, K, x, M, y, st};
+    return dispatch_type(qt, f);
+}
+
+}  // namespace wqk

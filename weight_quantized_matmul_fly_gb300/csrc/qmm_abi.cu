@@ -12,8 +12,12 @@ __device__ unsigned int g_status = 0;
 
 int launch_gemv(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int64_t M, float *y,
                 cudaStream_t st);
+int launch_gemv_tc(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int M, float *y,
+                   cudaStream_t st);
 int launch_mm(int qt, int tile, const void *wq, int64_t N, int64_t K, const void *x_bf16, int64_t M, float *y,
-              unsigned int *status, cudaStream_t st);
+              float *part, unsigned int *status, cudaStream_t st);
+size_t mm_partial_bytes(int64_t N, int64_t K, int64_t M);
+int mm_ksplit(int64_t N, int64_t K, int64_t M);
 int launch_x_to_bf16(const float *x, void *out, int64_t n, cudaStream_t st);
 int launch_mvid(int qt, bool xbf16, const void *const *wq, int64_t E, int64_t N, int64_t K, const void *x,
                 const int32_t *ids, int64_t M, int topk, float *y, unsigned int *status, cudaStream_t st);
@@ -59,29 +63,55 @@ unsigned int *status_ptr() {
     return cache[dev];
 }
 
+// The mat-vec path: quantized types on the tensor-core mat-vec kernel (16 tokens per launch at most,
+// halved when the activations of a K segment would not fit on chip); the plain types on the binary32 one.
+int run_matvec(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int64_t M, float *y,
+               cudaStream_t st) {
+    if (is_plain(qt)) return launch_gemv(qt, xbf16, wq, N, K, x, M, y, st);
+    const int esz = xbf16 ? 2 : 4;
+    for (int64_t m0 = 0; m0 < M;) {
+        int mg = (int)((M - m0) < 16 ? (M - m0) : 16);
+        int rc;
+        for (;;) {
+            rc = launch_gemv_tc(qt, xbf16, wq, N, K, static_cast<const uint8_t *>(x) + m0 * K * esz, mg,
+                                y + m0 * N, st);
+            if (rc != -3 || mg <= 4) break;
+            mg = (mg + 1) / 2;
+        }
+        if (rc) return rc == -3 ? QMM_EDIM : rc;
+        m0 += mg;
+    }
+    return 0;
+}
+
 inline size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
-// Scratch the tensor-core path needs: a bf16 copy of binary32 activations.
-size_t ws_bytes(int qtype, int64_t K, int64_t M, int path) {
-    if (path == 0 || (qtype & QMM_X_BF16)) return 0;
-    return align256((size_t)M * (size_t)K * 2);
+// Scratch the tensor-core path needs: a bf16 copy of binary32 activations, then the binary32 partial
+// sums of the K splits when K is split over CTAs.
+size_t ws_x_bytes(int qtype, int64_t K, int64_t M) {
+    return (qtype & QMM_X_BF16) ? 0 : align256((size_t)M * (size_t)K * 2);
+}
+size_t ws_bytes(int qtype, int64_t N, int64_t K, int64_t M, int path) {
+    if (path == 0) return 0;
+    return ws_x_bytes(qtype, K, M) + align256(mm_partial_bytes(N, K, M));
 }
 
 int run_mm(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, float *y, int tile,
            void *ws, size_t wsb, cudaStream_t st) {
     const int qt = qtype & 0xff;
+    const size_t need = ws_bytes(qtype, N, K, M, tile);
+    if (need && (!ws || wsb < need)) return QMM_EWORKSPACE;
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return QMM_EALIGN;
     const void *xb = x;
     if (!(qtype & QMM_X_BF16)) {
-        const size_t need = ws_bytes(qtype, K, M, tile);
-        if (!ws || wsb < need) return QMM_EWORKSPACE;
-        if (reinterpret_cast<uintptr_t>(ws) & 255u) return QMM_EALIGN;
         int rc = launch_x_to_bf16(static_cast<const float *>(x), ws, M * K, st);
         if (rc) return rc;
         xb = ws;
     }
+    float *part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ws_x_bytes(qtype, K, M));
     unsigned int *status = status_ptr();
     if (!status) return QMM_ECUDA;
-    return launch_mm(qt, tile, wq, N, K, xb, M, y, status, st);
+    return launch_mm(qt, tile, wq, N, K, xb, M, y, part, status, st);
 }
 
 }  // namespace
@@ -108,7 +138,7 @@ int qmm_pick_path(int qtype, int64_t N, int64_t K, int64_t M) {
 size_t qmm_workspace_size(int qtype, int64_t N, int64_t K, int64_t M) {
     const int path = qmm_pick_path(qtype, N, K, M);
     if (path <= 0) return 0;
-    return ws_bytes(qtype, K, M, path);
+    return ws_bytes(qtype, N, K, M, path);
 }
 
 int qmm_ws(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, float *y, void *workspace,
@@ -117,7 +147,7 @@ int qmm_ws(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64
     if (rc) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int path = qmm_pick_path(qtype, N, K, M);
-    if (path == 0) return launch_gemv(qtype & 0xff, (qtype & QMM_X_BF16) != 0, wq, N, K, x, M, y, st);
+    if (path == 0) return run_matvec(qtype & 0xff, (qtype & QMM_X_BF16) != 0, wq, N, K, x, M, y, st);
     return run_mm(wq, qtype, N, K, x, M, y, path, workspace, workspace_bytes, st);
 }
 
@@ -126,8 +156,8 @@ int qmm(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t 
     if (rc) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int path = qmm_pick_path(qtype, N, K, M);
-    if (path == 0) return launch_gemv(qtype & 0xff, (qtype & QMM_X_BF16) != 0, wq, N, K, x, M, y, st);
-    const size_t need = ws_bytes(qtype, K, M, path);
+    if (path == 0) return run_matvec(qtype & 0xff, (qtype & QMM_X_BF16) != 0, wq, N, K, x, M, y, st);
+    const size_t need = ws_bytes(qtype, N, K, M, path);
     void *ws = nullptr;
     if (need) {
         if (cudaMallocAsync(&ws, need, st) != cudaSuccess) return QMM_ECUDA;
@@ -142,10 +172,10 @@ int qmm_with_tile(const void *wq, int qtype, int64_t N, int64_t K, const void *x
     int rc = check_qmm(wq, qtype, N, K, x, M, y);
     if (rc) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (tile == 0) return launch_gemv(qtype & 0xff, (qtype & QMM_X_BF16) != 0, wq, N, K, x, M, y, st);
+    if (tile == 0) return run_matvec(qtype & 0xff, (qtype & QMM_X_BF16) != 0, wq, N, K, x, M, y, st);
     if (tile != 32 && tile != 64 && tile != 128) return QMM_ERANGE;
     if (!mm_eligible(qtype & 0xff, K)) return QMM_EBLOCK;
-    const size_t need = ws_bytes(qtype, K, M, tile);
+    const size_t need = ws_bytes(qtype, N, K, M, tile);
     void *ws = nullptr;
     if (need) {
         if (cudaMallocAsync(&ws, need, st) != cudaSuccess) return QMM_ECUDA;
@@ -212,6 +242,17 @@ int qmm_get_status(void *stream, unsigned int *status) {
     if (cudaStreamSynchronize(st) != cudaSuccess) return QMM_ECUDA;
     *status = v;
     return 0;
+}
+
+int qmm_launch_count(int qtype, int64_t N, int64_t K, int64_t M) {
+    const int path = qmm_pick_path(qtype, N, K, M);
+    if (path < 0) return path;
+    if (path == 0) {
+        // binary32 mat-vec for the plain types (16 tokens per launch), tensor-core mat-vec for the others
+        return (int)((M + 15) / 16);
+    }
+    const int S = mm_ksplit(N, K, M);
+    return ((qtype & QMM_X_BF16) ? 0 : 1) + 1 + (S > 1 ? 1 + ((M * N) % 4 ? 1 : 0) : 0);
 }
 
 const char *qmm_strerror(int code) {

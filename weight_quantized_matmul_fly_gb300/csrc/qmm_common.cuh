@@ -76,6 +76,10 @@ __device__ __forceinline__ uint4 ld_u128(const uint8_t *p) { return *reinterpret
 __device__ __forceinline__ uint32_t ld_u32_a2(const uint8_t *p) { return ld_u16(p) | (ld_u16(p + 2) << 16); }
 
 __device__ __forceinline__ float h2f(uint32_t bits) { return __half2float(__ushort_as_half((unsigned short)bits)); }
+// Exact integer -> binary32 for small magnitudes through the 2^23 (resp. 1.5 * 2^23) bias trick, which
+// runs on the full-rate ALU/FMA pipes instead of the conversion unit.
+__device__ __forceinline__ float u2f_small(uint32_t v) { return __int_as_float(0x4B000000 | v) - 8388608.0f; }  // v < 2^23
+__device__ __forceinline__ float i2f_small(int v) { return __int_as_float(0x4B400000 + v) - 12582912.0f; }    // |v| < 2^22
 __device__ __forceinline__ float bf2f(uint32_t bits) { return __uint_as_float(bits << 16); }
 
 // Load 32 consecutive bytes starting at a 2-byte aligned address into 8 words.
@@ -126,8 +130,8 @@ template <> struct Dec<T_Q4_0> {
 #pragma unroll
         for (int j = 0; j < 16; j++) {
             const uint32_t v = byte16(q, j);
-            w[j] = __fmul_rn(d, (float)((int)(v & 15u) - 8));
-            w[j + 16] = __fmul_rn(d, (float)((int)(v >> 4) - 8));
+            w[j] = __fmul_rn(d, i2f_small((int)(v & 15u) - 8));
+            w[j + 16] = __fmul_rn(d, i2f_small((int)(v >> 4) - 8));
         }
     }
 };
@@ -260,20 +264,20 @@ template <int QT> struct DecQ45K {
         const uint4 hd = ld_u128(b);         // d, dmin, 12 scale bytes
         const float d = h2f(hd.x & 0xffffu), dmin = h2f(hd.x >> 16);
         const uint32_t sc = six_bits(hd.y, hd.z, hd.w, t), mn = six_bits(hd.y, hd.z, hd.w, 8 + t);
-        const float ds = __fmul_rn(d, (float)sc), dm = __fmul_rn(dmin, (float)mn);
+        const float ds = __fmul_rn(d, u2f_small(sc)), dm = __fmul_rn(dmin, u2f_small(mn));
         uint32_t q[8];
         ld32_a16(b + (QT == T_Q4_K ? 16 : 48) + 32 * (t >> 1), q);
         const int sh = 4 * (t & 1);
         if (QT == T_Q4_K) {
 #pragma unroll
-            for (int l = 0; l < 32; l++) w[l] = __fmaf_rn(ds, (float)((byte_of(q, l) >> sh) & 15u), -dm);
+            for (int l = 0; l < 32; l++) w[l] = __fmaf_rn(ds, u2f_small((byte_of(q, l) >> sh) & 15u), -dm);
         } else {
             uint32_t qh[8];
             ld32_a16(b + 16, qh);
 #pragma unroll
             for (int l = 0; l < 32; l++) {
                 const uint32_t v = ((byte_of(q, l) >> sh) & 15u) | (((byte_of(qh, l) >> t) & 1u) << 4);
-                w[l] = __fmaf_rn(ds, (float)v, -dm);
+                w[l] = __fmaf_rn(ds, u2f_small(v), -dm);
             }
         }
     }
@@ -294,12 +298,12 @@ template <> struct Dec<T_Q6_K> {
         const int shl = 4 * (u >> 1), shh = 2 * u;
 #pragma unroll
         for (int half = 0; half < 2; half++) {
-            const float ds = __fmul_rn(d, (float)(int8_t)((sc2 >> (8 * half)) & 255u));
+            const float ds = __fmul_rn(d, i2f_small((int)(int8_t)((sc2 >> (8 * half)) & 255u)));
 #pragma unroll
             for (int l = 0; l < 16; l++) {
                 const int e = 16 * half + l;
                 const uint32_t v = ((byte_of(ql, e) >> shl) & 15u) | (((byte_of(qh, e) >> shh) & 3u) << 4);
-                w[e] = __fmul_rn(ds, (float)((int)v - 32));
+                w[e] = __fmul_rn(ds, i2f_small((int)v - 32));
             }
         }
     }
@@ -315,7 +319,7 @@ template <> struct Dec<T_A4G64> {
         uint32_t q[8];
         ld32_a4(b + 4, q);
 #pragma unroll
-        for (int l = 0; l < 32; l++) w[l] = __fmaf_rn(s, (float)((byte_of(q, l) >> sh) & 15u), bias);
+        for (int l = 0; l < 32; l++) w[l] = __fmaf_rn(s, u2f_small((byte_of(q, l) >> sh) & 15u), bias);
     }
 };
 

@@ -97,6 +97,34 @@ int qmm_ws(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64
            void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * qmm_noalloc: qmm() for callers that cannot allocate device memory. (The source pages have no
+ * counterpart; this entry point exists for users of the library.)
+ *
+ * Who needs it: code whose execution step must not call cudaMalloc / cudaMallocAsync, for example a
+ * plugin inside a framework that plans all device memory up front and forbids allocation while it runs,
+ * code with hard latency limits (an allocation can synchronize the device or wait on the driver), or a
+ * stream capture under a mode that rejects allocation calls. qmm() would allocate its tensor-core
+ * scratch there; qmm_ws() needs a buffer the caller may have no way to obtain.
+ *
+ * What it does: the same computation and kernels as qmm_ws(), with the scratch taken from one device
+ * array of QMM_NOALLOC_SCRATCH_BYTES that the library defines statically. The caller still passes wq, x
+ * and y as for qmm(). Nothing is allocated, on the host or the device.
+ *   - Limit: calls whose scratch (qmm_workspace_size) exceeds QMM_NOALLOC_SCRATCH_BYTES are refused with
+ *     QMM_EWORKSPACE before anything is launched (for binary32 activations roughly M*K*2 bytes plus
+ *     split-K partials; M*K up to about 30 million fits). Calls on the mat-vec path need no scratch.
+ *   - Every GPU that loads the library keeps the array (QMM_NOALLOC_SCRATCH_BYTES) until the process
+ *     exits.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that
+ *     device current; make that first call before any stream capture that should contain these calls.
+ *   - All calls share the one array and it keeps whatever the last call left there; no call relies on its
+ *     contents (every byte a call reads, that call wrote first). Calls whose kernels can overlap on the
+ *     GPU (different streams without ordering between them) race on the array: keep them ordered.
+ */
+#define QMM_NOALLOC_SCRATCH_BYTES (64u << 20)
+int qmm_noalloc(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, float *y,
+                void *stream);
+
+/*
  * qmm_id: expert-indexed mat-vec (MoE).  For each token t < M and slot j < topk, with e = ids[t*topk + j]:
  *     y[(t*topk + j)*N + n] = sum_k dequant(W_e)[n, k] * x[t*K + k]
  *   wq    HOST array of E device pointers, one N x K weight matrix of type qtype per expert

@@ -1,0 +1,65 @@
+"""qmm_noalloc: the allocation-free entry point, for callers that cannot allocate device memory while
+they run (its scratch lives in one device array the library owns).
+
+Checked through the C-ABI against qmm() on the same inputs, within the tolerance the parity tests use
+(the tensor-core class, 4e-3 * sum |w x| with the bound from the oracle), on two calls in a row with
+different inputs — the second call runs on whatever the first left in the shared array. Shapes cover the
+tensor-core path with and without the split-K partials, and the mat-vec path that needs no scratch.
+This file is collected last so that a failure here stops a run only after every other test has run.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+import weight_quantized_matmul_fly_gb300 as qmm
+from gpu_util import TOL_BF16, TOL_FP32, check_tol, dev, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    ("Q4_K", 9728, 2560, 512),   # tensor-core path, bf16 copy of x only
+    ("Q6_K", 1024, 2560, 100),   # tensor-core path with split-K partials
+    ("Q4_0", 256, 512, 7),       # mat-vec path: no scratch
+]
+
+
+@pytest.mark.parametrize("qtype,N,K,M", CASES)
+def test_noalloc_matches_qmm_twice(qtype, N, K, M):
+    torch = torch_cuda()
+    qmm.build()
+    need = qmm.qmm_workspace_size(qtype, N, K, M)
+    assert need <= qmm.NOALLOC_SCRATCH_BYTES
+    wq_h = oracle.quantize(qtype, synthetic.weights(N, K, seed=N + M))
+    wq = dev(wq_h)
+    tol = TOL_FP32 if M <= 16 else TOL_BF16
+    for call in range(2):
+        x_h = synthetic.activations(M, K, seed=100 * call + M)
+        x = dev(x_h)
+        y_ref = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        y_na = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        qmm.qmm(wq, qtype, N, K, x, y_ref)
+        qmm.qmm_noalloc(wq, qtype, N, K, x, y_na)
+        torch.cuda.synchronize()
+        a, b = y_na.cpu().numpy(), y_ref.cpu().numpy()
+        g = np.random.default_rng(call)
+        ms = g.integers(0, M, 200)
+        ns = g.integers(0, N, 200)
+        _, bnd = oracle.qmm_sampled(qtype, wq_h, N, K, x_h, ms, ns)
+        check_tol(a[ms, ns], b[ms, ns].astype(np.float64), bnd, tol, "noalloc vs qmm, call %d" % call)
+        assert np.all(np.isfinite(a))
+        # the same kernels run, so the results agree exactly as well
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_noalloc_refuses_oversized_scratch():
+    torch = torch_cuda()
+    qmm.build()
+    M, N, K = 8192, 128, 8192            # bf16 copy of x alone: 128 MiB
+    assert qmm.qmm_workspace_size("Q4_0", N, K, M) > qmm.NOALLOC_SCRATCH_BYTES
+    wq = torch.zeros(qmm.row_bytes("Q4_0", K) * N, dtype=torch.uint8, device="cuda")
+    x = torch.zeros((M, K), dtype=torch.float32, device="cuda")
+    y = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    with pytest.raises(qmm.QmmError) as e:
+        qmm.qmm_noalloc(wq, "Q4_0", N, K, x, y)
+    assert e.value.code == -8

@@ -12,7 +12,7 @@ import ctypes
 import os
 
 __all__ = ["QmmError", "TYPES", "TYPE_ID", "X_BF16", "build", "lib", "qmm", "qmm_ws", "qmm_workspace_size",
-           "qmm_launch_count",
+           "qmm_launch_count", "qmm_noalloc", "NOALLOC_SCRATCH_BYTES",
            "qmm_id", "qmm_with_tile", "qmm_pick_tile", "qmm_pick_path", "qmm_dequant", "qmm_quantize",
            "qmm_type_info", "qmm_get_status", "qmm_strerror", "row_bytes", "EXPORTS"]
 
@@ -26,8 +26,10 @@ X_BF16 = 0x100
 STATUS_BAD_ID, STATUS_TIMEOUT = 0x1, 0x2
 
 # Every symbol include/qmm.h declares.
-EXPORTS = ["qmm", "qmm_ws", "qmm_workspace_size", "qmm_id", "qmm_with_tile", "qmm_pick_tile", "qmm_pick_path",
-           "qmm_launch_count", "qmm_dequant", "qmm_quantize", "qmm_type_info", "qmm_get_status", "qmm_strerror"]
+EXPORTS = ["qmm", "qmm_ws", "qmm_workspace_size", "qmm_noalloc", "qmm_id", "qmm_with_tile", "qmm_pick_tile",
+           "qmm_pick_path", "qmm_launch_count", "qmm_dequant", "qmm_quantize", "qmm_type_info", "qmm_get_status",
+           "qmm_strerror"]
+NOALLOC_SCRATCH_BYTES = 64 << 20   # QMM_NOALLOC_SCRATCH_BYTES
 
 
 class QmmError(RuntimeError):
@@ -55,6 +57,7 @@ def lib():
         sig = {
             "qmm": ([P, I, I64, I64, P, I64, P, P], I),
             "qmm_ws": ([P, I, I64, I64, P, I64, P, P, SZ, P], I),
+            "qmm_noalloc": ([P, I, I64, I64, P, I64, P, P], I),
             "qmm_workspace_size": ([I, I64, I64, I64], SZ),
             "qmm_id": ([P, I64, I, I64, I64, P, P, I64, I, P, P], I),
             "qmm_with_tile": ([P, I, I64, I64, P, I64, P, I, P], I),
@@ -149,6 +152,16 @@ def qmm_ws(wq, qtype, N: int, K: int, x, y, workspace, stream=None):
     rc = lib().qmm_ws(_ptr(wq), _qt(qtype) | _xflag(x), int(N), int(K), _ptr(x), int(M), _ptr(y),
                       _ptr(workspace), nbytes, _stream(stream))
     _check(rc, "qmm_ws")
+    return y
+
+
+def qmm_noalloc(wq, qtype, N: int, K: int, x, y, stream=None):
+    """qmm() without any allocation: for callers that cannot allocate device memory while they run (the
+    scratch of the tensor-core path comes from one device array the library owns; see include/qmm.h)."""
+    M = x.shape[0]
+    rc = lib().qmm_noalloc(_ptr(wq), _qt(qtype) | _xflag(x), int(N), int(K), _ptr(x), int(M), _ptr(y),
+                           _stream(stream))
+    _check(rc, "qmm_noalloc")
     return y
 
 

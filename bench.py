@@ -184,8 +184,7 @@ def run_ours(args):
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
-    stream = torch.cuda.current_stream()
-    sptr = stream.cuda_stream
+    stream = torch.cuda.Stream()
     L = qmm.lib()
     import ctypes
     P = ctypes.c_void_p
@@ -193,51 +192,74 @@ def run_ours(args):
     ncalls = len(calls)
     per_step_launches = sum(qmm.qmm_launch_count(c[3], c[1], c[2], c[4]) for c in calls)
 
-    # raw argument tuples (C-ABI calls, no Python tensor work inside the timed loop)
-    raw = []
-    for copy in range(COPIES):
-        row = []
-        for name, N, K, qt, M, b in calls:
-            row.append((P(wq[(copy, name)].data_ptr()), qmm.TYPE_ID[qt], N, K, P(xs[(M, K, b)].data_ptr()), M,
-                        P(ys[(M, N)].data_ptr()), P(ws.data_ptr()), ws.numel(), P(sptr)))
-        raw.append(row)
+    # One CUDA graph per (weight copy, token-count group): the group's calls are captured back to back, so
+    # consecutive kernels overlap through programmatic dependent launch; events sit only between groups.
+    groups = []                                   # list of (label, [call indices])
+    for i, c in enumerate(calls):
+        label = "%dx%d" % (2, c[4]) if c[4] == BATCH2 else str(c[4])
+        if not groups or groups[-1][0] != label:
+            groups.append((label, []))
+        groups[-1][1].append(i)
 
-    def one_step(step, ev=None):
-        r = raw[step % COPIES]
-        for i, a in enumerate(r):
-            if ev is not None:
-                ev[2 * i].record(stream)
-            rc = L.qmm_ws(*a)
+    def run_group(copy, idxs):
+        for i in idxs:
+            name, N, K, qt, M, b = calls[i]
+            rc = L.qmm_ws(P(wq[(copy, name)].data_ptr()), qmm.TYPE_ID[qt], N, K, P(xs[(M, K, b)].data_ptr()), M,
+                          P(ys[(M, N)].data_ptr()), P(ws.data_ptr()), ws.numel(), P(stream.cuda_stream))
             if rc:
                 raise RuntimeError("qmm_ws: " + qmm.qmm_strerror(rc))
-            if ev is not None:
-                ev[2 * i + 1].record(stream)
 
-    for s in range(args.warmup):
-        one_step(s)
+    for s in range(args.warmup):                  # eager warm-up: kernel attributes, occupancy queries
+        for _, idxs in groups:
+            run_group(s % COPIES, idxs)
+    torch.cuda.synchronize()
+    graphs = {}
+    with torch.cuda.stream(stream):
+        for copy in range(COPIES):
+            for gi, (_, idxs) in enumerate(groups):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    run_group(copy, idxs)
+                graphs[(copy, gi)] = g
+    torch.cuda.synchronize()
+    for s in range(args.warmup):                  # warm-up replays
+        for gi in range(len(groups)):
+            graphs[(s % COPIES, gi)].replay()
     torch.cuda.synchronize()
 
-    # per-call events for a breakdown, recorded on the launching stream
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * ncalls)] for _ in range(args.steps)]
+    ng = len(groups)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(ng + 1)] for _ in range(args.steps)]
     t0e = torch.cuda.Event(enable_timing=True)
     t1e = torch.cuda.Event(enable_timing=True)
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
-    with Clocks(local) as clk:
-        t0e.record(stream)
-        for s in range(args.steps):
-            one_step(args.warmup + s, evs[s])
-        t1e.record(stream)
-        torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        with Clocks(local) as clk:
+            t0e.record(stream)
+            for s in range(args.steps):
+                copy = (args.warmup + s) % COPIES
+                for gi in range(ng):
+                    evs[s][gi].record(stream)
+                    graphs[(copy, gi)].replay()
+                evs[s][ng].record(stream)
+            t1e.record(stream)
+            torch.cuda.synchronize()
     if pg:
         pg.barrier()
     total_ms = max_over_ranks(pg, t0e.elapsed_time(t1e), dev)
-    per_call = np.zeros((args.steps, ncalls))
+    group_ms = np.zeros(ng)
     for s in range(args.steps):
-        for i in range(ncalls):
-            per_call[s, i] = evs[s][2 * i].elapsed_time(evs[s][2 * i + 1])
-    call_ms = per_call.mean(axis=0)
+        for gi in range(ng):
+            group_ms[gi] += evs[s][gi].elapsed_time(evs[s][gi + 1])
+    group_ms /= args.steps
+    # per-call times are not measured inside a group; spread each group's time over its calls by weight
+    # bytes for the per-call table only (the aggregates below use group times)
+    call_ms = np.zeros(ncalls)
+    for gi, (_, idxs) in enumerate(groups):
+        wbs = np.array([weight_bytes(calls[i][1], calls[i][2], calls[i][3]) for i in idxs])
+        for i, wbi in zip(idxs, wbs):
+            call_ms[i] = group_ms[gi] * wbi / wbs.sum()
 
     # aggregates
     small = [i for i, c in enumerate(calls) if c[4] <= 16]
@@ -281,11 +303,12 @@ def run_ours(args):
         del d["wbytes"], d["flops"]
 
     if args.detail:
-        for i, c in enumerate(calls):
-            wb = weight_bytes(c[1], c[2], c[3])
-            print("%-12s M=%-5d b=%d %9.2f us %8.1f GB/s %8.2f TFLOP/s" % (
-                c[0], c[4], c[5], call_ms[i] * 1e3, wb / (call_ms[i] * 1e-3) / 1e9,
-                2.0 * c[4] * c[1] * c[2] / (call_ms[i] * 1e-3) / 1e12), file=sys.stderr)
+        for gi, (label, idxs) in enumerate(groups):
+            wb = sum(weight_bytes(calls[i][1], calls[i][2], calls[i][3]) for i in idxs)
+            fl = sum(2.0 * calls[i][4] * calls[i][1] * calls[i][2] for i in idxs)
+            print("M=%-6s %2d calls %9.2f us %8.1f GB/s %8.2f TFLOP/s" % (
+                label, len(idxs), group_ms[gi] * 1e3, wb / (group_ms[gi] * 1e-3) / 1e9,
+                fl / (group_ms[gi] * 1e-3) / 1e12), file=sys.stderr)
     e2e = run_e2e(args, qmm, torch, dev, calls, wq, ws) if not args.case else None
     cpu = cpu_baseline(args) if (rank == 0 and world == 1 and not args.no_cpu and not args.case) else None
 
@@ -410,7 +433,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--case", default=None, help="time one call only, e.g. ffn_gate:2048")

@@ -365,8 +365,18 @@ template <int NT, bool XBF16> struct Layout {
     static constexpr int TOK = XBF16 ? 8 * NT : 4 * NT;   // tokens served
     static constexpr int WARPS = 8;
     __host__ __device__ static int xs_stride(int kpad) { return kpad + 16; }   // elements; +32 B breaks bank aliasing
-    __host__ __device__ static size_t bytes(int kpad, int unit) {
-        return (size_t)COLS * xs_stride(kpad) * 2 + (size_t)TOK * (kpad / unit) * 4 + (size_t)WARPS * 16 * TOK * 4;
+    // Columns actually staged: with one column group only those the tokens use (a power of two; the MMA
+    // reads the others from a used column and their results are never read).
+    __host__ __device__ static int staged_cols(int M) {
+        if (NT > 1) return COLS;
+        const int need = XBF16 ? M : 2 * M;
+        int c = 2;
+        while (c < need) c *= 2;
+        return c < COLS ? c : COLS;
+    }
+    __host__ __device__ static size_t bytes(int kpad, int unit, int M) {
+        return (size_t)staged_cols(M) * xs_stride(kpad) * 2 + (size_t)TOK * (kpad / unit) * 4 +
+               (size_t)WARPS * 16 * TOK * 4;
     }
 };
 
@@ -390,7 +400,7 @@ __device__ __forceinline__ float ld_dsmem_f32(const float *local, uint32_t rank)
 template <int QT, int NT, bool XBF16, bool FULL>
 __device__ __forceinline__ void macro_step(const typename Frag<QT>::Raw &cur0, const typename Frag<QT>::Raw &cur1,
                                            const __nv_bfloat16 *xs, int xst, const float *sx, int sxs, int kloc,
-                                           int nvalid, int g, int t, float (&acc)[NT][4]) {
+                                           int nvalid, int g, int t, int colmask, float (&acc)[NT][4]) {
     using F = Frag<QT>;
     constexpr int UNIT = F::UNIT, GPU = UNIT / 16;
     // types without an additive term (w = ds * (q - bias))
@@ -410,7 +420,8 @@ __device__ __forceinline__ void macro_step(const typename Frag<QT>::Raw &cur0, c
         const int xo = kloc + F::xoff(u, t);
 #pragma unroll
         for (int mt = 0; mt < NT; ++mt) {
-            const uint2 b = *reinterpret_cast<const uint2 *>(xs + (size_t)(8 * mt + g) * xst + xo);
+            const int col = NT == 1 ? (g & colmask) : 8 * mt + g;
+            const uint2 b = *reinterpret_cast<const uint2 *>(xs + (size_t)col * xst + xo);
             if ((u % GPU) == 0) {
                 const float z[4] = {0.f, 0.f, 0.f, 0.f};
                 mma_bf16_16816(d[mt], a, b.x, b.y, z);
@@ -471,8 +482,10 @@ __global__ void __launch_bounds__(256, 2)
     const int64_t ke = (kb + kseg < K) ? kb + kseg : K;
     const int kpad = kseg;                            // multiple of 256
     const int xst = LY::xs_stride(kpad), sxs = kpad / UNIT;
+    const int scols = LY::staged_cols(M);
+    const int colmask = scols - 1;                    // NT == 1: staged columns are a power of two
     __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(smem);
-    float *sx = reinterpret_cast<float *>(smem + (size_t)LY::COLS * xst * 2);
+    float *sx = reinterpret_cast<float *>(smem + (size_t)scols * xst * 2);
     float *part = sx + (size_t)TOK * sxs;             // [WARPS][16][TOK]
 
     const int tid = threadIdx.x;
@@ -563,10 +576,10 @@ __global__ void __launch_bounds__(256, 2)
         }
         const int kloc = (int)(mb * 256 - kb);    // position of this macro block in the segment
         if (mb < full_end) {
-            macro_step<QT, NT, XBF16, true>(cur0, cur1, xs, xst, sx, sxs, kloc, 16, g, t, acc);
+            macro_step<QT, NT, XBF16, true>(cur0, cur1, xs, xst, sx, sxs, kloc, 16, g, t, colmask, acc);
         } else {
             macro_step<QT, NT, XBF16, false>(cur0, cur1, xs, xst, sx, sxs, kloc, (int)((K - mb * 256) / 16), g, t,
-                                             acc);
+                                             colmask, acc);
         }
         cur0 = nxt0;
         cur1 = nxt1;
@@ -625,22 +638,62 @@ __global__ void __launch_bounds__(256, 2)
 // ------------------------------------------------------------------------------------------ host side
 namespace {
 
+// CTAs of this kernel instance that can be resident at once when launched in clusters of S (S = 1: no
+// cluster), for a given dynamic shared memory size; queried once per (S, size class) and cached.
+template <int QT, int NT, bool XBF16, int KW>
+int64_t gtc_capacity(int64_t S, size_t smem) {
+    using LY = gtc::Layout<NT, XBF16>;
+    auto kern = gtc::gemv_tc_kernel<QT, NT, XBF16, KW>;
+    static int64_t cache[9][4] = {};   // [S][smem class: <=16K, <=48K, <=100K, other]
+    const int cls = smem <= 16 * 1024 ? 0 : (smem <= 48 * 1024 ? 1 : (smem <= 100 * 1024 ? 2 : 3));
+    if (S < 1 || S > 8) return 0;
+    if (cache[S][cls]) return cache[S][cls];
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024) != cudaSuccess)
+            return 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess) return 0;
+        attr_set = true;
+    }
+    const size_t smem_q = cls == 0 ? 16 * 1024 : (cls == 1 ? 48 * 1024 : 100 * 1024);
+    int64_t cap = 0;
+    if (S == 1) {
+        int per_sm = 0, dev = 0, sms = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, LY::WARPS * 32, smem_q) == cudaSuccess)
+            cap = (int64_t)per_sm * sms;
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, (unsigned)S, 1);
+        cfg.blockDim = dim3(LY::WARPS * 32, 1, 1);
+        cfg.dynamicSmemBytes = smem_q;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = (unsigned)S;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int nclusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) == cudaSuccess) cap = (int64_t)nclusters * S;
+    }
+    if (cap <= 0) cap = S;          // unknown: assume one cluster at a time rather than fail
+    cache[S][cls] = cap;
+    return cap;
+}
+
 template <int QT, int NT, bool XBF16, int KW>
 int launch_gtc_kw(const void *wq, int64_t N, int64_t K, const void *x, int M, float *y, int64_t S, int64_t kseg,
                   cudaStream_t st) {
     using LY = gtc::Layout<NT, XBF16>;
     constexpr int UNIT = gtc::Frag<QT>::UNIT, RG = LY::WARPS / KW;
     auto kern = gtc::gemv_tc_kernel<QT, NT, XBF16, KW>;
-    static bool attr_set = false;   // once per kernel instance
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024) != cudaSuccess)
-            return -6;
-        attr_set = true;
-    }
+    if (gtc_capacity<QT, NT, XBF16, KW>(1, 0) <= 0) return -6;   // also sets the kernel's attributes
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((N + 16 * RG - 1) / (16 * RG)), (unsigned)S, 1);
     cfg.blockDim = dim3(LY::WARPS * 32, 1, 1);
-    cfg.dynamicSmemBytes = LY::bytes((int)kseg, UNIT);
+    cfg.dynamicSmemBytes = LY::bytes((int)kseg, UNIT, M);
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -656,47 +709,51 @@ int launch_gtc_kw(const void *wq, int64_t N, int64_t K, const void *x, int M, fl
     return e == cudaSuccess ? 0 : -6;
 }
 
-// Work split: row groups of 16 x K slices, aiming at about `target` warps in flight (a full wave of
-// 2 CTAs x 8 warps per SM), K slices of at least one macro block, at most 8 CTAs per cluster and a
-// shared-memory budget for the staged activations.
+// Work split. The CTAs of one launch should fit in one wave (resident CTAs as the occupancy calculator
+// reports them, clusters included: a cluster must fit on one GPC, which strands slots): a second, partial
+// wave doubles the time of these short kernels. Among the
+// (K slices per CTA, K segments per cluster) choices that fit, take the one that leaves each warp the
+// fewest macro blocks to stream; larger M keeps more row groups per CTA so that the activations each CTA
+// stages stay small next to its weights.
 template <int QT, int NT, bool XBF16>
 int launch_gtc_t(const void *wq, int64_t N, int64_t K, const void *x, int M, float *y, cudaStream_t st) {
     using LY = gtc::Layout<NT, XBF16>;
     constexpr int UNIT = gtc::Frag<QT>::UNIT;
-    static int sms = 0;
-    if (!sms) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (sms <= 0) sms = 148;
-    }
-    const int64_t target = (int64_t)sms * 16;
     const int64_t ngroups = (N + 15) / 16;
     const int64_t nmacro = (K + 255) / 256;
-    int64_t slices = (target + ngroups - 1) / ngroups;            // K slices wanted per row group
-    if (slices > nmacro) slices = nmacro;
-    if (slices > 64) slices = 64;
-    if (slices < 1) slices = 1;
-    // Each CTA stages its K segment of the activations, so the activation bytes a CTA reads grow with M
-    // while its weight bytes grow with its rows: larger M keeps more row groups (fewer K slices) per CTA.
     const int kw_cap = M <= 2 ? 8 : (M <= 8 ? 2 : 1);
-    int kw = 1;
-    while (kw < kw_cap && kw * 2 <= slices) kw *= 2;
-    int64_t S = (slices + kw - 1) / kw;
-    if (S > 8) S = 8;
-    // shared-memory budget: the CTA stages its whole K segment of activations
-    int64_t kseg = ((nmacro + S - 1) / S) * 256;
-    while (LY::bytes((int)kseg, UNIT) > 100 * 1024) {
-        if (S >= 8) return -3;                                    // caller splits the tokens
-        ++S;
-        kseg = ((nmacro + S - 1) / S) * 256;
+    int best_kw = 1, best_s = 1;
+    int64_t best_cost = -1, best_ctas = 0;
+    for (int kw = 1; kw <= kw_cap; kw *= 2) {
+        const int64_t nrb = (ngroups + (8 / kw) - 1) / (8 / kw);
+        for (int64_t S = 1; S <= 8 && S <= nmacro; ++S) {
+            const int64_t kseg = ((nmacro + S - 1) / S) * 256;
+            if ((K + kseg - 1) / kseg != S) continue;                 // S segments must all be non-empty
+            if (LY::bytes((int)kseg, UNIT, M) > 100 * 1024) continue;
+            const int64_t ctas = nrb * S;
+            const size_t smem = LY::bytes((int)kseg, UNIT, M);
+            int64_t resident;
+            switch (kw) {
+            case 1: resident = gtc_capacity<QT, NT, XBF16, 1>(S, smem); break;
+            case 2: resident = gtc_capacity<QT, NT, XBF16, 2>(S, smem); break;
+            case 4: resident = gtc_capacity<QT, NT, XBF16, 4>(S, smem); break;
+            default: resident = gtc_capacity<QT, NT, XBF16, 8>(S, smem); break;
+            }
+            const int64_t waves = (ctas + resident - 1) / resident;
+            const int64_t per_warp = (kseg / 256 + kw - 1) / kw;      // macro blocks per warp
+            const int64_t cost = waves * (per_warp + 1);              // +1: per-CTA staging and reduction
+            if (best_cost < 0 || cost < best_cost || (cost == best_cost && ctas > best_ctas)) {
+                best_cost = cost; best_kw = kw; best_s = (int)S; best_ctas = ctas;
+            }
+        }
     }
-    S = (K + kseg - 1) / kseg;
-    switch (kw) {
-    case 1: return launch_gtc_kw<QT, NT, XBF16, 1>(wq, N, K, x, M, y, S, kseg, st);
-    case 2: return launch_gtc_kw<QT, NT, XBF16, 2>(wq, N, K, x, M, y, S, kseg, st);
-    case 4: return launch_gtc_kw<QT, NT, XBF16, 4>(wq, N, K, x, M, y, S, kseg, st);
-    default: return launch_gtc_kw<QT, NT, XBF16, 8>(wq, N, K, x, M, y, S, kseg, st);
+    if (best_cost < 0) return -3;                                     // caller splits the tokens
+    const int64_t kseg = ((nmacro + best_s - 1) / best_s) * 256;
+    switch (best_kw) {
+    case 1: return launch_gtc_kw<QT, NT, XBF16, 1>(wq, N, K, x, M, y, best_s, kseg, st);
+    case 2: return launch_gtc_kw<QT, NT, XBF16, 2>(wq, N, K, x, M, y, best_s, kseg, st);
+    case 4: return launch_gtc_kw<QT, NT, XBF16, 4>(wq, N, K, x, M, y, best_s, kseg, st);
+    default: return launch_gtc_kw<QT, NT, XBF16, 8>(wq, N, K, x, M, y, best_s, kseg, st);
     }
 }
 

@@ -47,6 +47,149 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// ------------------------------------------------------------------------------------------ slab decoders
+// A decoder lane turns 32 consecutive weights of one row (chunk c) into 16 bf16x2 words, each the bf16
+// rounding (nearest even) of the binary32 dequantized weight. Raw bytes are loaded one K step ahead.
+// Small codes become binary32 through the 2^23 bias: byte-permute the code under exponent byte 0x4B,
+// subtract 2^23 (exact), then one multiply-add.
+__device__ __forceinline__ float code_f(uint32_t v4, int j) {   // byte j of v4 (< 2^8) as binary32
+    return __int_as_float(__byte_perm(v4, 0x4B000000u, 0x7540u + (uint32_t)j)) - 8388608.0f;
+}
+__device__ __forceinline__ void fma4_pack(uint32_t v4, float s, float o, uint32_t &lo, uint32_t &hi) {
+    lo = pack_bf16x2(__fmaf_rn(s, code_f(v4, 0), o), __fmaf_rn(s, code_f(v4, 1), o));
+    hi = pack_bf16x2(__fmaf_rn(s, code_f(v4, 2), o), __fmaf_rn(s, code_f(v4, 3), o));
+}
+
+template <int QT> struct Slab {
+    static constexpr bool FAST = false;
+    struct Raw { int dummy; };
+};
+
+// Q4_K / Q5_K: chunk t of a 256-weight super-block = sub-block t; its 32 codes are the low (t even) or
+// high (t odd) nibbles of qs[32*(t/2) .. +31], with the fifth bit of Q5_K in bit t of qh[0..31].
+template <int QT> struct SlabQ45K {
+    static constexpr bool FAST = true;
+    struct Raw { uint4 hd, q0, q1, h0, h1; };
+    __device__ static void load(Raw &r, const uint8_t *row, int c) {
+        constexpr int BY = QT == T_Q4_K ? 144 : 176, QOFF = QT == T_Q4_K ? 16 : 48;
+        const uint8_t *b = row + BY * (c >> 3);
+        const int t = c & 7;
+        r.hd = ld_u128(b);
+        r.q0 = ld_u128(b + QOFF + 32 * (t >> 1));
+        r.q1 = ld_u128(b + QOFF + 32 * (t >> 1) + 16);
+        if (QT == T_Q5_K) { r.h0 = ld_u128(b + 16); r.h1 = ld_u128(b + 32); }
+    }
+    __device__ static void decode(const Raw &r, int c, uint32_t (&o)[16]) {
+        const int t = c & 7, sh = 4 * (t & 1);
+        const float d = h2f(r.hd.x & 0xffffu), dmin = h2f(r.hd.x >> 16);
+        const float ds = __fmul_rn(d, u2f_small(six_bits(r.hd.y, r.hd.z, r.hd.w, t)));
+        const float dm = -__fmul_rn(dmin, u2f_small(six_bits(r.hd.y, r.hd.z, r.hd.w, 8 + t)));
+        const uint32_t q[8] = {r.q0.x, r.q0.y, r.q0.z, r.q0.w, r.q1.x, r.q1.y, r.q1.z, r.q1.w};
+        const uint32_t hh[8] = {r.h0.x, r.h0.y, r.h0.z, r.h0.w, r.h1.x, r.h1.y, r.h1.z, r.h1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t v = (q[i] >> sh) & 0x0F0F0F0Fu;
+            if (QT == T_Q5_K) v |= ((hh[i] >> t) & 0x01010101u) << 4;
+            fma4_pack(v, ds, dm, o[2 * i], o[2 * i + 1]);
+        }
+    }
+};
+template <> struct Slab<T_Q4_K> : SlabQ45K<T_Q4_K> {};
+template <> struct Slab<T_Q5_K> : SlabQ45K<T_Q5_K> {};
+
+// Q6_K: chunk t (sub-blocks 2t, 2t+1) takes 32 consecutive ql bytes and 32 consecutive qh bytes. A block
+// (210 bytes) starts 4-byte aligned or 2 bytes past it: in the second case each 4-byte word is rebuilt
+// from the two aligned words around it.
+template <> struct Slab<T_Q6_K> {
+    static constexpr bool FAST = true;
+    struct Raw { uint32_t ql[9], qh[9]; uint32_t sc; uint32_t d; uint32_t a2; };
+    __device__ static void load(Raw &r, const uint8_t *row, int c) {
+        const uint8_t *b = row + 210 * (c >> 3);
+        const int t = c & 7, h = t >> 2, u = t & 3;
+        const uint8_t *pl = b + 64 * h + 32 * (u & 1), *ph = b + 128 + 32 * h;
+        r.a2 = (reinterpret_cast<uintptr_t>(b) & 3u) != 0;
+        if (!r.a2) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) { r.ql[i] = ld_u32(pl + 4 * i); r.qh[i] = ld_u32(ph + 4 * i); }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 9; ++i) { r.ql[i] = ld_u32(pl - 2 + 4 * i); r.qh[i] = ld_u32(ph - 2 + 4 * i); }
+        }
+        r.sc = ld_u16(b + 192 + 2 * t);
+        r.d = ld_u16(b + 208);
+    }
+    __device__ static void decode(const Raw &r, int c, uint32_t (&o)[16]) {
+        const int t = c & 7, u = t & 3;
+        const int shl = 4 * (u >> 1), shh = 2 * u;
+        const float d = h2f(r.d);
+        const float ds0 = __fmul_rn(d, i2f_small((int)(int8_t)(r.sc & 255u)));
+        const float ds1 = __fmul_rn(d, i2f_small((int)(int8_t)(r.sc >> 8)));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t wl = r.a2 ? __funnelshift_r(r.ql[i], r.ql[i + 1], 16) : r.ql[i];
+            const uint32_t wh = r.a2 ? __funnelshift_r(r.qh[i], r.qh[i + 1], 16) : r.qh[i];
+            const uint32_t v = ((wl >> shl) & 0x0F0F0F0Fu) | (((wh >> shh) & 0x03030303u) << 4);
+            // (q - 32) * ds: the bias is folded into the subtraction of 2^23 + 32 (exact)
+            const float s = i < 4 ? ds0 : ds1;
+            const float f0 = __int_as_float(__byte_perm(v, 0x4B000000u, 0x7540u)) - 8388640.0f;
+            const float f1 = __int_as_float(__byte_perm(v, 0x4B000000u, 0x7541u)) - 8388640.0f;
+            const float f2 = __int_as_float(__byte_perm(v, 0x4B000000u, 0x7542u)) - 8388640.0f;
+            const float f3 = __int_as_float(__byte_perm(v, 0x4B000000u, 0x7543u)) - 8388640.0f;
+            o[2 * i] = pack_bf16x2(__fmul_rn(s, f0), __fmul_rn(s, f1));
+            o[2 * i + 1] = pack_bf16x2(__fmul_rn(s, f2), __fmul_rn(s, f3));
+        }
+    }
+};
+
+// A4G64: chunk c is half of a 64-weight block: low (c even) or high (c odd) nibbles of its 32 code bytes.
+template <> struct Slab<T_A4G64> {
+    static constexpr bool FAST = true;
+    struct Raw { uint32_t sb; uint32_t q[8]; };
+    __device__ static void load(Raw &r, const uint8_t *row, int c) {
+        const uint8_t *b = row + 36 * (c >> 1);
+        r.sb = ld_u32(b);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) r.q[i] = ld_u32(b + 4 + 4 * i);
+    }
+    __device__ static void decode(const Raw &r, int c, uint32_t (&o)[16]) {
+        const int sh = 4 * (c & 1);
+        const float s = bf2f(r.sb & 0xffffu), bias = bf2f(r.sb >> 16);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) fma4_pack((r.q[i] >> sh) & 0x0F0F0F0Fu, s, bias, o[2 * i], o[2 * i + 1]);
+    }
+};
+
+// Q4_0: chunk c is block c (18 bytes, 2-byte aligned): 16 code bytes, low nibbles first.
+template <> struct Slab<T_Q4_0> {
+    static constexpr bool FAST = true;
+    struct Raw { uint32_t q[4]; uint32_t d; };
+    __device__ static void load(Raw &r, const uint8_t *row, int c) {
+        const uint8_t *b = row + 18 * c;
+        r.d = ld_u16(b);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) r.q[i] = ld_u16(b + 2 + 4 * i) | (ld_u16(b + 4 + 4 * i) << 16);
+    }
+    __device__ static void decode(const Raw &r, int c, uint32_t (&o)[16]) {
+        (void)c;
+        const float d = h2f(r.d);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            // (q - 8) * d, the bias folded into the subtraction of 2^23 + 8
+            const uint32_t lo = r.q[i] & 0x0F0F0F0Fu, hi = (r.q[i] >> 4) & 0x0F0F0F0Fu;
+            float f[4], g[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                f[j] = __fmul_rn(d, __int_as_float(__byte_perm(lo, 0x4B000000u, 0x7540u + j)) - 8388616.0f);
+                g[j] = __fmul_rn(d, __int_as_float(__byte_perm(hi, 0x4B000000u, 0x7540u + j)) - 8388616.0f);
+            }
+            o[2 * i] = pack_bf16x2(f[0], f[1]);
+            o[2 * i + 1] = pack_bf16x2(f[2], f[3]);
+            o[8 + 2 * i] = pack_bf16x2(g[0], g[1]);
+            o[8 + 2 * i + 1] = pack_bf16x2(g[2], g[3]);
+        }
+    }
+};
+
 struct Smem {
     uint64_t full_b[STAGES], full_a[STAGES], empty[STAGES], done;
     uint32_t tmem;
@@ -146,34 +289,55 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int d = warp - 2;
         const int r_local = 16 * d + (lane >> 1), h = lane & 1;
         const int row = n0 + r_local;
-        const uint8_t *wrow = wq + (int64_t)(row < N ? row : N - 1) * rowbytes;
+        const bool row_ok = row < N;
+        const uint8_t *wrow = wq + (int64_t)(row_ok ? row : N - 1) * rowbytes;
         const int nchunks = (int)((K + 31) / 32);
         const uint32_t sA_u32 = ptx::smem_u32(sA);
+        using SL = Slab<QT>;
+        // raw bytes of the next two K steps are in flight while a step is decoded
+        typename SL::Raw r0, r1, r2;
+        if constexpr (SL::FAST) {
+            const int c0 = 2 * kbeg + h;
+            if (nsteps > 0 && c0 < nchunks) SL::load(r0, wrow, c0);
+            if (nsteps > 1 && c0 + 2 < nchunks) SL::load(r1, wrow, c0 + 2);
+        }
         for (int i = 0; i < nsteps; ++i) {
             const int s = i % STAGES;
+            const int c = 2 * (kbeg + i) + h;
+            if constexpr (SL::FAST) {
+                if (i + 2 < nsteps && c + 4 < nchunks) SL::load(r2, wrow, c + 4);
+            }
             if (i >= STAGES && !ptx::mbar_wait(&sm->empty[s], ((i / STAGES) - 1) & 1, status)) {
                 sm->abort = 1;
                 break;
             }
             if (*(volatile int *)&sm->abort) break;
-            const int c = 2 * (kbeg + i) + h;
-            float w[32];
-            if (row < N && c < nchunks) {
-                decode_chunk<QT>(wrow, c, K, w);
+            uint32_t o[16];
+            if (row_ok && c < nchunks) {
+                if constexpr (SL::FAST) {
+                    SL::decode(r0, c, o);
+                } else {
+                    float w[32];
+                    decode_chunk<QT>(wrow, c, K, w);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) o[j] = pack_bf16x2(w[2 * j], w[2 * j + 1]);
+                }
             } else {
 #pragma unroll
-                for (int l = 0; l < 32; ++l) w[l] = 0.0f;
+                for (int j = 0; j < 16; ++j) o[j] = 0u;
             }
             const uint32_t a_base = sA_u32 + s * A_STAGE;
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                ptx::st_shared_v4(a_base + sw128_off(r_local, 4 * h + p), pack_bf16x2(w[8 * p + 0], w[8 * p + 1]),
-                                  pack_bf16x2(w[8 * p + 2], w[8 * p + 3]), pack_bf16x2(w[8 * p + 4], w[8 * p + 5]),
-                                  pack_bf16x2(w[8 * p + 6], w[8 * p + 7]));
-            }
+            for (int p = 0; p < 4; ++p)
+                ptx::st_shared_v4(a_base + sw128_off(r_local, 4 * h + p), o[4 * p], o[4 * p + 1], o[4 * p + 2],
+                                  o[4 * p + 3]);
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&sm->full_a[s]);
+            if constexpr (SL::FAST) {
+                r0 = r1;
+                r1 = r2;
+            }
         }
         // ---------------- epilogue: TMEM lanes = weight rows, columns = tokens
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
@@ -338,13 +502,13 @@ struct MmLaunch {
 }  // namespace
 
 // K split of the tensor-core path, a function of (N, K, M) only (never of the token tile), so that every
-// tile variant adds the same partial sums: split while CTAs of 128 rows x 256 tokens leave more than
-// half the SMs idle, keeping at least 8 K steps per split.
+// tile variant adds the same partial sums: split while CTAs of 128 rows x 256 tokens do not fill the
+// GPU's SMs once, keeping at least 4 K steps per split.
 int mm_ksplit(int64_t N, int64_t K, int64_t M) {
     const int64_t ksteps = (K + mm::BK - 1) / mm::BK;
     const int64_t ctas = ((N + mm::BM - 1) / mm::BM) * ((M + 255) / 256);
     int64_t S = 1;
-    while (ctas * S * 2 <= 148 && ksteps / (S * 2) >= 8 && S < 16) S *= 2;
+    while (ctas * S < 152 && ksteps / (S * 2) >= 4 && S < 32) S *= 2;
     return (int)S;
 }
 

@@ -502,14 +502,33 @@ struct MmLaunch {
 }  // namespace
 
 // K split of the tensor-core path, a function of (N, K, M) only (never of the token tile), so that every
-// tile variant adds the same partial sums: split while CTAs of 128 rows x 256 tokens do not fill the
-// GPU's SMs once, keeping at least 4 K steps per split.
+// tile variant adds the same partial sums. CTAs of 128 rows x 256 tokens run in waves of one per SM; a
+// split S multiplies the CTAs and divides each CTA's K steps, and costs S*M*N*4 bytes of partial sums
+// written and read back. The split minimises
+//     ceil(ctas * S / SMs) * ceil(ksteps / S) * t_step  +  (2 S M N * 4 bytes) / HBM bandwidth
+// with t_step about 0.5 us (one K step of a full CTA) and splits of at least 4 K steps.
 int mm_ksplit(int64_t N, int64_t K, int64_t M) {
     const int64_t ksteps = (K + mm::BK - 1) / mm::BK;
     const int64_t ctas = ((N + mm::BM - 1) / mm::BM) * ((M + 255) / 256);
-    int64_t S = 1;
-    while (ctas * S < 152 && ksteps / (S * 2) >= 4 && S < 32) S *= 2;
-    return (int)S;
+    static int nsm = 0;   // SMs of the current device, queried once
+    if (!nsm) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0)
+            nsm = 148;
+    }
+    const double sms = (double)nsm, t_step_us = 0.5, hbm_bytes_per_us = 6.0e6;
+    int best = 1;
+    double best_t = -1.0;
+    for (int S = 1; S <= 32; ++S) {
+        if (S > 1 && ksteps / S < 4) break;
+        const int64_t waves = (int64_t)((ctas * S + (int64_t)sms - 1) / (int64_t)sms);
+        const int64_t steps = (ksteps + S - 1) / S;
+        double t = (double)waves * (double)steps * t_step_us;
+        if (S > 1) t += 2.0 * S * (double)M * (double)N * 4.0 / hbm_bytes_per_us;
+        if (best_t < 0 || t < best_t * 0.98) { best_t = t; best = S; }
+    }
+    return best;
 }
 
 // Partial buffers of the K splits are M*N binary32 each, padded to a multiple of 4 elements so that every

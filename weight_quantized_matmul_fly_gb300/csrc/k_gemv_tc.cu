@@ -21,12 +21,15 @@
 // number of 4- or 8-token column groups (tiny-llm PR 122, "perf: Optimize quantized matmul for small
 // decode batches": the x_size buckets become column-group buckets).
 //
-// Work split. A CTA owns 16 rows per warp and one K segment; the K segments of a row block form a thread
-// block cluster, whose CTAs add their partial sums through distributed shared memory in a fixed order
-// (so the result is deterministic and no global scratch is needed).
+// Work split. A CTA owns 16 rows per row group and one K segment; the K segments of a row block form a
+// thread block cluster. Each CTA stores its partial sums into the shared memory of the cluster's first
+// CTA, which adds them in rank order after one cluster barrier (so the result is deterministic and no
+// global scratch is needed). The weights reach shared memory through bulk copies issued before the
+// kernel waits for its predecessor (programmatic dependent launch), so consecutive launches overlap.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "ptx.cuh"
 #include "qmm_common.cuh"
 
 namespace wqk {
@@ -358,12 +361,30 @@ __device__ __forceinline__ void frag_codes(const typename Frag<QT>::Raw &r, int 
 }
 
 // ------------------------------------------------------------------------------------------ the kernel
-// Shared memory: activations of the CTA's K segment as bf16 columns (xs), per-unit activation sums (sx)
-// and the partial results that the warps of a CTA, then the CTAs of a cluster, add up (part).
+// Shared memory, in order: the warps' mbarriers (NSMAX per warp), the weight ring (per warp NS stages of
+// 16 rows x one macro block, one row per SLOT bytes), the activations of the CTA's K segment as bf16
+// columns (xs), per-unit activation sums (sx), and the partial results that the warps of a CTA, then the
+// CTAs of a cluster, add up (part).
+constexpr int NSMAX = 8;
+// Bytes of one row's macro block in a ring stage. A bulk copy must start and end on 16-byte boundaries, so
+// a stage row holds the 16-byte-aligned range around the macro block: at most 15 bytes more on each side.
+// An odd number of 16-byte units spreads the 8 rows a warp load touches over distinct banks.
+template <int QT> __host__ __device__ constexpr int slot_bytes() {
+    constexpr int B = (256 / TypeInfo<QT>::QK) * TypeInfo<QT>::BYTES;
+    constexpr int S = (B + 15 + 15) / 16 * 16;
+    return (S / 16) % 2 ? S : S + 16;
+}
+// Row stride of the resident tile for a segment of `seg` bytes per row: room for the 16-byte-aligned range
+// around it, an odd number of 16-byte units.
+__host__ __device__ inline int resident_stride(int seg) {
+    const int s = (seg + 15 + 15) / 16 * 16;
+    return (s / 16) % 2 ? s : s + 16;
+}
 template <int NT, bool XBF16> struct Layout {
     static constexpr int COLS = 8 * NT;              // MMA columns
     static constexpr int TOK = XBF16 ? 8 * NT : 4 * NT;   // tokens served
     static constexpr int WARPS = 8;
+    static constexpr int BARS = WARPS * NSMAX * 8;
     __host__ __device__ static int xs_stride(int kpad) { return kpad + 16; }   // elements; +32 B breaks bank aliasing
     // Columns actually staged: with one column group only those the tokens use (a power of two; the MMA
     // reads the others from a used column and their results are never read).
@@ -374,9 +395,18 @@ template <int NT, bool XBF16> struct Layout {
         while (c < need) c *= 2;
         return c < COLS ? c : COLS;
     }
-    __host__ __device__ static size_t bytes(int kpad, int unit, int M) {
+    // activations, unit sums and partials
+    __host__ __device__ static size_t xbytes(int kpad, int unit, int M) {
         return (size_t)staged_cols(M) * xs_stride(kpad) * 2 + (size_t)TOK * (kpad / unit) * 4 +
                (size_t)WARPS * 16 * TOK * 4;
+    }
+    __host__ __device__ static size_t ring_bytes(int slot, int ns) { return (size_t)WARPS * ns * 16 * slot; }
+    // cluster reduction slots in rank 0: S slots of RG x 16 rows x TOK tokens
+    __host__ __device__ static size_t red_bytes(int S, int rg) { return S > 1 ? (size_t)S * rg * 16 * TOK * 4 : 0; }
+    // resident mode: RG row groups of 16 rows, `seg` bytes each
+    __host__ __device__ static size_t tile_bytes(int rg, int seg) { return (size_t)rg * 16 * resident_stride(seg); }
+    __host__ __device__ static size_t bytes(int kpad, int unit, int M, int slot, int ns) {
+        return BARS + ring_bytes(slot, ns) + xbytes(kpad, unit, M);
     }
 };
 
@@ -388,12 +418,19 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ float ld_dsmem_f32(const float *local, uint32_t rank) {
+// Split cluster barrier: arrive (relaxed) early, wait later.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+// Address of `local` (a shared memory location of this CTA) in the CTA of the cluster with rank `rank`.
+__device__ __forceinline__ uint32_t dsmem_addr(const void *local, uint32_t rank) {
     uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local)), ra;
-    float v;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
-    return v;
+    return ra;
+}
+__device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
 // One macro block of two rows into the accumulators. FULL: all 16 groups lie inside K.
@@ -464,10 +501,22 @@ __device__ __forceinline__ void macro_step(const typename Frag<QT>::Raw &cur0, c
 
 // CTA: 8 warps = RG row groups of 16 rows x KW slices of the CTA's K segment; the cluster's S CTAs take
 // consecutive K segments of the same rows.
+//
+// Weight stream, in one of two modes; in both the weights go to shared memory by bulk copies
+// (cp.async.bulk) that lanes 0-15 of a warp issue, one per row, each arriving on an mbarrier with its byte
+// count, and the copies are issued before the kernel waits for its predecessor in the stream, so that
+// the weight stream of this launch overlaps the end of the previous one.
+//   resident (ns == 0): the CTA's whole tile (its rows x its K segment) fits in shared memory. Warp
+//     (rg, 0) copies each of its row group's 16 rows in one piece, all at once; the KW warps of the row
+//     group wait on the group's mbarrier and decode their macro blocks from the tile.
+//   ring (ns > 0): each warp streams its 16 rows through its own ring of `ns` stages of one macro block:
+//     it waits on a stage's mbarrier, decodes the stage and refills it with the macro block `ns` steps
+//     ahead. Used when the tile does not fit.
+// Few large copies stream faster than many small ones, which is why the resident mode is preferred.
 template <int QT, int NT, bool XBF16, int KW>
 __global__ void __launch_bounds__(256, 2)
     gemv_tc_kernel(const uint8_t *__restrict__ wq, int N, int64_t K, int64_t rowbytes, const void *__restrict__ x,
-                   int M, float *__restrict__ y, int kseg) {
+                   int M, float *__restrict__ y, int kseg, int ns, unsigned int *__restrict__ status) {
     using F = Frag<QT>;
     using LY = Layout<NT, XBF16>;
     constexpr int WARPS = LY::WARPS, RG = WARPS / KW;
@@ -475,6 +524,7 @@ __global__ void __launch_bounds__(256, 2)
     constexpr int TOK = LY::TOK;
     constexpr int QK = TypeInfo<QT>::QK, BYTES = TypeInfo<QT>::BYTES;
     constexpr int BPM = 256 / QK;                     // blocks per macro block
+    constexpr int SLOT = slot_bytes<QT>();
     extern __shared__ __align__(16) uint8_t smem[];
 
     const int S = gridDim.y;
@@ -484,81 +534,152 @@ __global__ void __launch_bounds__(256, 2)
     const int xst = LY::xs_stride(kpad), sxs = kpad / UNIT;
     const int scols = LY::staged_cols(M);
     const int colmask = scols - 1;                    // NT == 1: staged columns are a power of two
-    __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(smem);
-    float *sx = reinterpret_cast<float *>(smem + (size_t)scols * xst * 2);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    uint8_t *ring = smem + LY::BARS;
+    __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(
+        ring + (ns == 0 ? LY::tile_bytes(RG, kseg / 256 * BPM * BYTES) : LY::ring_bytes(SLOT, ns)));
+    float *sx = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(xs) + (size_t)scols * xst * 2);
     float *part = sx + (size_t)TOK * sxs;             // [WARPS][16][TOK]
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
     const int rg = warp / KW, ks = warp % KW;
     const int nrow0 = blockIdx.x * (16 * RG) + 16 * rg;
-    const int r0 = nrow0 + g, r1 = nrow0 + g + 8;
-    const uint8_t *row0 = wq + (int64_t)(r0 < N ? r0 : N - 1) * rowbytes;
-    const uint8_t *row1 = wq + (int64_t)(r1 < N ? r1 : N - 1) * rowbytes;
     // this warp's macro blocks: a balanced share of the segment's
     const int64_t smb = kb / 256, nmb = (ke - kb + 255) / 256;
     const int64_t mb_beg = smb + (nmb * ks) / KW, mb_end = smb + (nmb * (ks + 1)) / KW;
+    const int nsteps = (int)(mb_end - mb_beg);
     const int64_t nblocks_row = K / QK;
     const int64_t full_end = K / 256;                 // macro blocks lying entirely inside K
-
-    // The weights are read before waiting for the preceding kernel in the stream (they are model data
-    // that no kernel of this library writes); activations and outputs only after.
-    typename F::Raw cur0, cur1, nxt0, nxt1;
     auto nblk_of = [&](int64_t mb) {
         const int64_t r = nblocks_row - mb * BPM;
         return (int)(r < BPM ? r : BPM);
     };
-    if (mb_beg < mb_end) {
-        F::load(cur0, row0 + mb_beg * BPM * BYTES, t, nblk_of(mb_beg));
-        F::load(cur1, row1 + mb_beg * BPM * BYTES, t, nblk_of(mb_beg));
+
+    uint64_t *wbar = bars + warp * NSMAX;             // this warp's stage barriers (ring mode)
+    uint64_t *gbar = bars + rg * NSMAX;                // the row group's tile barrier (resident mode)
+    uint8_t *wring = ring + (size_t)warp * ns * 16 * SLOT;
+    const bool resident = ns == 0;
+    const int rstride = resident_stride(kseg / 256 * BPM * BYTES);
+    uint8_t *gtile = ring + (size_t)rg * 16 * rstride;  // resident mode: row group rg's 16 rows
+    // Lane l < 16 copies row nrow0 + l (clamped to the last row; the rows past N are never stored).
+    const int crow = nrow0 + (lane & 15) < N ? nrow0 + (lane & 15) : N - 1;
+    const uintptr_t wend = reinterpret_cast<uintptr_t>(wq) + (uintptr_t)N * (uintptr_t)rowbytes;
+    auto issue = [&](int step) {
+        const int slot = step % ns;
+        if (lane < 16) {
+            const int64_t mb = mb_beg + step;
+            const uintptr_t a = reinterpret_cast<uintptr_t>(wq + (int64_t)crow * rowbytes + mb * BPM * BYTES);
+            const uintptr_t e = a + (uintptr_t)nblk_of(mb) * BYTES;
+            const uintptr_t a0 = a & ~(uintptr_t)15;
+            uintptr_t e1 = (e + 15) & ~(uintptr_t)15;
+            if (e1 > wend) e1 = wend & ~(uintptr_t)15;  // the buffer's last bytes, past its last 16-byte boundary
+            uint8_t *dst = wring + (size_t)(slot * 16 + (lane & 15)) * SLOT;
+            for (uintptr_t q = e1 > a0 ? e1 : a0; q < e; ++q) dst[q - a0] = *reinterpret_cast<const uint8_t *>(q);
+            ptx::fence_proxy_async_smem();           // earlier generic reads of the stage before the async write
+            ptx::mbar_arrive_expect_tx(&wbar[slot], e1 > a0 ? (uint32_t)(e1 - a0) : 0u);
+            if (e1 > a0) ptx::bulk_load(dst, reinterpret_cast<const void *>(a0), (uint32_t)(e1 - a0), &wbar[slot]);
+        }
+    };
+    // Rows g and g + 8 of a stage start where the copy put them: at the data's offset within 16 bytes.
+    const uintptr_t radr0 = reinterpret_cast<uintptr_t>(wq + (int64_t)(nrow0 + g < N ? nrow0 + g : N - 1) * rowbytes);
+    const uintptr_t radr1 =
+        reinterpret_cast<uintptr_t>(wq + (int64_t)(nrow0 + g + 8 < N ? nrow0 + g + 8 : N - 1) * rowbytes);
+
+    // The weights are requested before waiting for the preceding kernel in the stream (they are model data
+    // that no kernel of this library writes); activations and outputs are touched only after.
+    if (lane == 0)
+        for (int i = 0; i < ns; ++i) ptx::mbar_init(&wbar[i], 16);
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (resident) {
+        // one copy per row: the segment's blocks of that row (warps with ks > 0 only wait for them)
+        if (ks == 0) {
+            if (lane == 0) ptx::mbar_init(gbar, 16);
+            ptx::fence_mbar_init();
+            __syncwarp();
+            if (lane < 16) {
+                const uintptr_t a = reinterpret_cast<uintptr_t>(wq + (int64_t)crow * rowbytes + smb * BPM * BYTES);
+                const int64_t sblocks = (nblocks_row - smb * BPM) < (int64_t)(kseg / QK) ? nblocks_row - smb * BPM
+                                                                                         : (int64_t)(kseg / QK);
+                const uintptr_t e = a + (uintptr_t)sblocks * BYTES;
+                const uintptr_t a0 = a & ~(uintptr_t)15;
+                uintptr_t e1 = (e + 15) & ~(uintptr_t)15;
+                if (e1 > wend) e1 = wend & ~(uintptr_t)15;
+                uint8_t *dst = gtile + (size_t)lane * rstride;
+                for (uintptr_t q = e1 > a0 ? e1 : a0; q < e; ++q) dst[q - a0] = *reinterpret_cast<const uint8_t *>(q);
+                ptx::mbar_arrive_expect_tx(gbar, e1 > a0 ? (uint32_t)(e1 - a0) : 0u);
+                if (e1 > a0) ptx::bulk_load(dst, reinterpret_cast<const void *>(a0), (uint32_t)(e1 - a0), gbar);
+            }
+        }
+    } else {
+        const int npre = nsteps < ns ? nsteps : ns;
+        for (int i = 0; i < npre; ++i) issue(i);
     }
+    if (gridDim.y > 1) cluster_arrive_relaxed();      // matched by the wait before the partials move
     asm volatile("griddepcontrol.launch_dependents;");
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // ---- stage this segment's activations (tokens < M): bf16 columns and per-unit sums
+    // ---- stage this segment's activations (tokens < M): bf16 columns and per-unit sums. The loads of XU
+    //      iterations are issued together so that their latencies overlap.
     {
+        constexpr int XU = 4, STEP = WARPS * 32;
         const int k4n = kpad / 4;
         const int mtok = M < TOK ? M : TOK;
-        for (int idx = tid; idx < mtok * k4n; idx += WARPS * 32) {
-            const int tok = idx / k4n, k4 = idx - tok * k4n;
-            const int64_t k = kb + 4 * k4;
-            float v[4] = {0.f, 0.f, 0.f, 0.f};
-            if (k < ke) {
+        const int total = mtok * k4n;                 // a multiple of 64: the loop below is warp-uniform
+        for (int base = tid; base < total; base += XU * STEP) {
+            float v[XU][4];
+#pragma unroll
+            for (int j = 0; j < XU; ++j) {
+                const int idx = base + j * STEP;
+                const int tok = idx / k4n, k4 = idx - tok * k4n;
+                const int64_t k = kb + 4 * k4;
+                v[j][0] = v[j][1] = v[j][2] = v[j][3] = 0.0f;
+                if (idx < total && k < ke) {
+                    if constexpr (XBF16) {
+                        const uint2 p = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(x) +
+                                                                              (int64_t)tok * K + k));
+                        v[j][0] = __uint_as_float(p.x << 16); v[j][1] = __uint_as_float(p.x & 0xffff0000u);
+                        v[j][2] = __uint_as_float(p.y << 16); v[j][3] = __uint_as_float(p.y & 0xffff0000u);
+                    } else {
+                        const float4 p = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(x) +
+                                                                               (int64_t)tok * K + k));
+                        v[j][0] = p.x; v[j][1] = p.y; v[j][2] = p.z; v[j][3] = p.w;
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < XU; ++j) {
+                const int idx = base + j * STEP;
+                if (idx >= total) break;
+                const int tok = idx / k4n, k4 = idx - tok * k4n;
                 if constexpr (XBF16) {
-                    const uint2 p = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(x) +
-                                                                          (int64_t)tok * K + k));
-                    v[0] = __uint_as_float(p.x << 16); v[1] = __uint_as_float(p.x & 0xffff0000u);
-                    v[2] = __uint_as_float(p.y << 16); v[3] = __uint_as_float(p.y & 0xffff0000u);
+                    __nv_bfloat162 h0 = __floats2bfloat162_rn(v[j][0], v[j][1]),
+                                   h1 = __floats2bfloat162_rn(v[j][2], v[j][3]);
+                    *reinterpret_cast<uint2 *>(xs + (size_t)tok * xst + 4 * k4) =
+                        make_uint2(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1));
                 } else {
-                    const float4 p = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(x) +
-                                                                           (int64_t)tok * K + k));
-                    v[0] = p.x; v[1] = p.y; v[2] = p.z; v[3] = p.w;
-                }
-            }
-            if constexpr (XBF16) {
-                __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]), h1 = __floats2bfloat162_rn(v[2], v[3]);
-                *reinterpret_cast<uint2 *>(xs + (size_t)tok * xst + 4 * k4) =
-                    make_uint2(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1));
-            } else {
-                float hi[4], lo[4];
+                    float hi[4], lo[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    hi[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
-                    lo[j] = __fsub_rn(v[j], hi[j]);
+                    for (int i = 0; i < 4; ++i) {
+                        hi[i] = __bfloat162float(__float2bfloat16_rn(v[j][i]));
+                        lo[i] = __fsub_rn(v[j][i], hi[i]);
+                    }
+                    __nv_bfloat162 h0 = __floats2bfloat162_rn(hi[0], hi[1]), h1 = __floats2bfloat162_rn(hi[2], hi[3]);
+                    __nv_bfloat162 l0 = __floats2bfloat162_rn(lo[0], lo[1]), l1 = __floats2bfloat162_rn(lo[2], lo[3]);
+                    const int col = 8 * (tok >> 2) + 2 * (tok & 3);
+                    *reinterpret_cast<uint2 *>(xs + (size_t)col * xst + 4 * k4) =
+                        make_uint2(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1));
+                    *reinterpret_cast<uint2 *>(xs + (size_t)(col + 1) * xst + 4 * k4) =
+                        make_uint2(*reinterpret_cast<uint32_t *>(&l0), *reinterpret_cast<uint32_t *>(&l1));
                 }
-                __nv_bfloat162 h0 = __floats2bfloat162_rn(hi[0], hi[1]), h1 = __floats2bfloat162_rn(hi[2], hi[3]);
-                __nv_bfloat162 l0 = __floats2bfloat162_rn(lo[0], lo[1]), l1 = __floats2bfloat162_rn(lo[2], lo[3]);
-                const int col = 8 * (tok >> 2) + 2 * (tok & 3);
-                *reinterpret_cast<uint2 *>(xs + (size_t)col * xst + 4 * k4) =
-                    make_uint2(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1));
-                *reinterpret_cast<uint2 *>(xs + (size_t)(col + 1) * xst + 4 * k4) =
-                    make_uint2(*reinterpret_cast<uint32_t *>(&l0), *reinterpret_cast<uint32_t *>(&l1));
-            }
-            // per-unit sums of x (binary32, original values), reduced over the UNIT/4 lanes of a unit
-            float s = (v[0] + v[1]) + (v[2] + v[3]);
+                // per-unit sums of x (binary32, original values), reduced over the UNIT/4 lanes of a unit
+                float sum = (v[j][0] + v[j][1]) + (v[j][2] + v[j][3]);
 #pragma unroll
-            for (int off = 1; off < UNIT / 4; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-            if ((k4 & (UNIT / 4 - 1)) == 0) sx[tok * sxs + (4 * k4) / UNIT] = s;
+                for (int off = 1; off < UNIT / 4; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                if ((k4 & (UNIT / 4 - 1)) == 0) sx[tok * sxs + (4 * k4) / UNIT] = sum;
+            }
         }
     }
     __syncthreads();
@@ -569,11 +690,26 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[mt][j] = 0.0f;
 
-    for (int64_t mb = mb_beg; mb < mb_end; ++mb) {
-        if (mb + 1 < mb_end) {
-            F::load(nxt0, row0 + (mb + 1) * BPM * BYTES, t, nblk_of(mb + 1));
-            F::load(nxt1, row1 + (mb + 1) * BPM * BYTES, t, nblk_of(mb + 1));
+    typename F::Raw cur0, cur1;
+    int done = 0;                                     // stages consumed (a timed-out wait stops the stream)
+    for (; done < nsteps; ++done) {
+        const int64_t mb = mb_beg + done;
+        const uint8_t *p0, *p1;
+        if (resident) {
+            if (done == 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(gbar, 0u, status))) break;
+            const uintptr_t so = (uintptr_t)(smb * BPM * BYTES);          // the segment's first byte in a row
+            const size_t jo = (size_t)(mb - smb) * BPM * BYTES;           // this macro block within the segment
+            p0 = gtile + (size_t)g * rstride + ((radr0 + so) & 15) + jo;
+            p1 = gtile + (size_t)(g + 8) * rstride + ((radr1 + so) & 15) + jo;
+        } else {
+            const int slot = done % ns;
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&wbar[slot], (uint32_t)((done / ns) & 1), status))) break;
+            const uintptr_t mo = (uintptr_t)(mb * BPM * BYTES);
+            p0 = wring + (size_t)(slot * 16 + g) * SLOT + ((radr0 + mo) & 15);
+            p1 = wring + (size_t)(slot * 16 + g + 8) * SLOT + ((radr1 + mo) & 15);
         }
+        F::load(cur0, p0, t, nblk_of(mb));
+        F::load(cur1, p1, t, nblk_of(mb));
         const int kloc = (int)(mb * 256 - kb);    // position of this macro block in the segment
         if (mb < full_end) {
             macro_step<QT, NT, XBF16, true>(cur0, cur1, xs, xst, sx, sxs, kloc, 16, g, t, colmask, acc);
@@ -581,9 +717,15 @@ __global__ void __launch_bounds__(256, 2)
             macro_step<QT, NT, XBF16, false>(cur0, cur1, xs, xst, sx, sxs, kloc, (int)((K - mb * 256) / 16), g, t,
                                              colmask, acc);
         }
-        cur0 = nxt0;
-        cur1 = nxt1;
+        if (!resident) {
+            __syncwarp();
+            if (done + ns < nsteps) issue(done + ns);
+        }
     }
+    // After a timeout: wait (bounded) for the copies still in flight before the shared memory is released.
+    if (!resident)
+        for (int i = done + 1; i < nsteps && i < done + ns; ++i)
+            ptx::mbar_wait(&wbar[i % ns], (uint32_t)((i / ns) & 1), status);
 
     // ---- results. binary32 x: acc[mt][0] = (row g, token 4mt+t), acc[mt][2] = (row g+8, token 4mt+t);
     //      bf16 x: acc[mt][0/1] = (row g, tokens 8mt+2t, +1), acc[mt][2/3] = (row g+8, same tokens).
@@ -601,35 +743,42 @@ __global__ void __launch_bounds__(256, 2)
         }
     }
     __syncthreads();
-    // add the KW slices (fixed order) into the first slice's partials
+    // Add the KW slices (fixed order). With a cluster, every CTA then stores its sums into rank 0's
+    // shared memory (slot = its rank), one cluster barrier makes them visible, and rank 0 adds the S slots
+    // in rank order.
     const int mtok = M < TOK ? M : TOK;
-    for (int idx = tid; idx < RG * 16 * mtok; idx += WARPS * 32) {
+    const int nres = RG * 16 * mtok;
+    float *red = part + (size_t)WARPS * 16 * TOK;     // [S][nres], used in rank 0 (cluster launches only)
+    uint32_t rank = 0, red0 = 0;
+    if (S > 1) {
+        cluster_wait();                               // every CTA of the cluster has started
+        rank = cluster_rank();
+        red0 = dsmem_addr(red, 0);
+    }
+    for (int idx = tid; idx < nres; idx += WARPS * 32) {
         const int r = idx / mtok, tk = idx - r * mtok;     // r: row within the CTA
         const int rgi = r >> 4, rr = r & 15;
-        float s = 0.0f;
+        float sum = 0.0f;
 #pragma unroll
-        for (int q = 0; q < KW; ++q) s += part[((size_t)(rgi * KW + q) * 16 + rr) * TOK + tk];
+        for (int q = 0; q < KW; ++q) sum += part[((size_t)(rgi * KW + q) * 16 + rr) * TOK + tk];
         if (S == 1) {
             const int n = blockIdx.x * (16 * RG) + r;
-            if (n < N) y[(int64_t)tk * N + n] = s;
+            if (n < N) y[(int64_t)tk * N + n] = sum;
         } else {
-            part[((size_t)(rgi * KW) * 16 + rr) * TOK + tk] = s;
+            st_dsmem_f32(red0 + 4u * (rank * (uint32_t)nres + (uint32_t)idx), sum);
         }
     }
     if (S > 1) {
         cluster_sync();
-        if (cluster_rank() == 0) {
-            for (int idx = tid; idx < RG * 16 * mtok; idx += WARPS * 32) {
+        if (rank == 0) {
+            for (int idx = tid; idx < nres; idx += WARPS * 32) {
                 const int r = idx / mtok, tk = idx - r * mtok;
-                const int rgi = r >> 4, rr = r & 15;
-                const float *src = &part[((size_t)(rgi * KW) * 16 + rr) * TOK + tk];
-                float s = 0.0f;
-                for (int q = 0; q < S; ++q) s += ld_dsmem_f32(src, (uint32_t)q);
+                float sum = 0.0f;
+                for (int q = 0; q < S; ++q) sum += red[q * nres + idx];
                 const int n = blockIdx.x * (16 * RG) + r;
-                if (n < N) y[(int64_t)tk * N + n] = s;
+                if (n < N) y[(int64_t)tk * N + n] = sum;
             }
         }
-        cluster_sync();
     }
 }
 
@@ -638,24 +787,29 @@ __global__ void __launch_bounds__(256, 2)
 // ------------------------------------------------------------------------------------------ host side
 namespace {
 
+// Shared memory a CTA may take: two CTAs fit on an SM (228 KB), so one CTA of the next launch in the
+// stream can start streaming its weights while one of this launch still runs.
+constexpr size_t kSmemCap = 110 * 1024;
+
 // CTAs of this kernel instance that can be resident at once when launched in clusters of S (S = 1: no
-// cluster), for a given dynamic shared memory size; queried once per (S, size class) and cached.
+// cluster), for a given dynamic shared memory size; queried once per (S, 4 KB size class) and cached.
 template <int QT, int NT, bool XBF16, int KW>
 int64_t gtc_capacity(int64_t S, size_t smem) {
     using LY = gtc::Layout<NT, XBF16>;
     auto kern = gtc::gemv_tc_kernel<QT, NT, XBF16, KW>;
-    static int64_t cache[9][4] = {};   // [S][smem class: <=16K, <=48K, <=100K, other]
-    const int cls = smem <= 16 * 1024 ? 0 : (smem <= 48 * 1024 ? 1 : (smem <= 100 * 1024 ? 2 : 3));
-    if (S < 1 || S > 8) return 0;
+    constexpr int NCLS = (int)(kSmemCap / 4096) + 1;
+    static int64_t cache[9][NCLS] = {};
+    const int cls = (int)((smem + 4095) / 4096);
+    if (S < 1 || S > 8 || cls >= NCLS) return 0;
     if (cache[S][cls]) return cache[S][cls];
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024) != cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap) != cudaSuccess)
             return 0;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess) return 0;
         attr_set = true;
     }
-    const size_t smem_q = cls == 0 ? 16 * 1024 : (cls == 1 ? 48 * 1024 : 100 * 1024);
+    const size_t smem_q = (size_t)cls * 4096;
     int64_t cap = 0;
     if (S == 1) {
         int per_sm = 0, dev = 0, sms = 0;
@@ -685,7 +839,7 @@ int64_t gtc_capacity(int64_t S, size_t smem) {
 
 template <int QT, int NT, bool XBF16, int KW>
 int launch_gtc_kw(const void *wq, int64_t N, int64_t K, const void *x, int M, float *y, int64_t S, int64_t kseg,
-                  cudaStream_t st) {
+                  int ns, unsigned int *status, cudaStream_t st) {
     using LY = gtc::Layout<NT, XBF16>;
     constexpr int UNIT = gtc::Frag<QT>::UNIT, RG = LY::WARPS / KW;
     auto kern = gtc::gemv_tc_kernel<QT, NT, XBF16, KW>;
@@ -693,7 +847,11 @@ int launch_gtc_kw(const void *wq, int64_t N, int64_t K, const void *x, int M, fl
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((N + 16 * RG - 1) / (16 * RG)), (unsigned)S, 1);
     cfg.blockDim = dim3(LY::WARPS * 32, 1, 1);
-    cfg.dynamicSmemBytes = LY::bytes((int)kseg, UNIT, M);
+    constexpr int MB_BYTES = 256 / TypeInfo<QT>::QK * TypeInfo<QT>::BYTES;
+    cfg.dynamicSmemBytes = (ns == 0 ? LY::BARS + LY::tile_bytes(RG, (int)(kseg / 256 * MB_BYTES)) +
+                                          LY::xbytes((int)kseg, UNIT, M)
+                                    : LY::bytes((int)kseg, UNIT, M, gtc::slot_bytes<QT>(), ns)) +
+                           LY::red_bytes((int)S, RG);
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -705,56 +863,73 @@ int launch_gtc_kw(const void *wq, int64_t N, int64_t K, const void *x, int M, fl
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t *>(wq), (int)N, K, row_bytes(QT, K), x,
-                                       M, y, (int)kseg);
+                                       M, y, (int)kseg, ns, status);
     return e == cudaSuccess ? 0 : -6;
 }
 
 // Work split. The CTAs of one launch should fit in one wave (resident CTAs as the occupancy calculator
 // reports them, clusters included: a cluster must fit on one GPC, which strands slots): a second, partial
-// wave doubles the time of these short kernels. Among the
-// (K slices per CTA, K segments per cluster) choices that fit, take the one that leaves each warp the
-// fewest macro blocks to stream; larger M keeps more row groups per CTA so that the activations each CTA
-// stages stay small next to its weights.
+// wave doubles the time of these short kernels. Among the (K slices per CTA, K segments per cluster)
+// choices that fit, take the one that leaves each warp the fewest macro blocks to stream (counting a
+// cluster and a ring as one macro block more each, as measured on the layer shapes); larger M keeps
+// more row groups per CTA so that the activations each CTA stages stay small next to its weights. Each
+// warp's ring takes as many stages as the shared memory left over allows (at most its macro blocks).
 template <int QT, int NT, bool XBF16>
-int launch_gtc_t(const void *wq, int64_t N, int64_t K, const void *x, int M, float *y, cudaStream_t st) {
+int launch_gtc_t(const void *wq, int64_t N, int64_t K, const void *x, int M, float *y, unsigned int *status,
+                 cudaStream_t st) {
     using LY = gtc::Layout<NT, XBF16>;
-    constexpr int UNIT = gtc::Frag<QT>::UNIT;
+    constexpr int UNIT = gtc::Frag<QT>::UNIT, SLOT = gtc::slot_bytes<QT>();
+    constexpr int MB_BYTES = 256 / TypeInfo<QT>::QK * TypeInfo<QT>::BYTES;   // bytes of a macro block
     const int64_t ngroups = (N + 15) / 16;
     const int64_t nmacro = (K + 255) / 256;
-    const int kw_cap = M <= 2 ? 8 : (M <= 8 ? 2 : 1);
-    int best_kw = 1, best_s = 1;
+    // K slices per CTA: more for fewer tokens (the staged activations are then small); only the counts
+    // that some M of this column-group count can use are compiled.
+    constexpr int KWMAX = NT == 1 ? 8 : ((NT == 2 && !XBF16) ? 2 : 1);
+    int kw_cap = M <= 2 ? 8 : (M <= 8 ? 2 : 1);
+    if (kw_cap > KWMAX) kw_cap = KWMAX;
+    int best_kw = 1, best_s = 1, best_ns = 1;
     int64_t best_cost = -1, best_ctas = 0;
     for (int kw = 1; kw <= kw_cap; kw *= 2) {
         const int64_t nrb = (ngroups + (8 / kw) - 1) / (8 / kw);
         for (int64_t S = 1; S <= 8 && S <= nmacro; ++S) {
             const int64_t kseg = ((nmacro + S - 1) / S) * 256;
             if ((K + kseg - 1) / kseg != S) continue;                 // S segments must all be non-empty
-            if (LY::bytes((int)kseg, UNIT, M) > 100 * 1024) continue;
-            const int64_t ctas = nrb * S;
-            const size_t smem = LY::bytes((int)kseg, UNIT, M);
-            int64_t resident;
-            switch (kw) {
-            case 1: resident = gtc_capacity<QT, NT, XBF16, 1>(S, smem); break;
-            case 2: resident = gtc_capacity<QT, NT, XBF16, 2>(S, smem); break;
-            case 4: resident = gtc_capacity<QT, NT, XBF16, 4>(S, smem); break;
-            default: resident = gtc_capacity<QT, NT, XBF16, 8>(S, smem); break;
+            const int64_t per_warp = (kseg / 256 + kw - 1) / kw;      // macro blocks per warp (at most)
+            const size_t fixed = LY::BARS + LY::xbytes((int)kseg, UNIT, M) + LY::red_bytes((int)S, 8 / kw);
+            const size_t tile = LY::tile_bytes(8 / kw, (int)(kseg / 256 * MB_BYTES));
+            int64_t ns = 0;                                           // resident tile if it fits
+            size_t smem = fixed + tile;
+            if (smem > kSmemCap) {
+                if (fixed + LY::ring_bytes(SLOT, 1) > kSmemCap) continue;
+                ns = (int64_t)((kSmemCap - fixed) / LY::ring_bytes(SLOT, 1));
+                if (ns > per_warp) ns = per_warp;
+                if (ns > gtc::NSMAX) ns = gtc::NSMAX;
+                if (ns < 2 && per_warp >= 2) continue;                // no overlap of copies and decoding
+                smem = LY::bytes((int)kseg, UNIT, M, SLOT, (int)ns) + LY::red_bytes((int)S, 8 / kw);
             }
+            const int64_t ctas = nrb * S;
+            int64_t resident = 0;
+            if (kw == 1) resident = gtc_capacity<QT, NT, XBF16, 1>(S, smem);
+            if constexpr (KWMAX >= 2) if (kw == 2) resident = gtc_capacity<QT, NT, XBF16, 2>(S, smem);
+            if constexpr (KWMAX >= 4) if (kw == 4) resident = gtc_capacity<QT, NT, XBF16, 4>(S, smem);
+            if constexpr (KWMAX >= 8) if (kw == 8) resident = gtc_capacity<QT, NT, XBF16, 8>(S, smem);
+            if (resident <= 0) continue;
             const int64_t waves = (ctas + resident - 1) / resident;
-            const int64_t per_warp = (kseg / 256 + kw - 1) / kw;      // macro blocks per warp
-            const int64_t cost = waves * (per_warp + 1);              // +1: per-CTA staging and reduction
+            // In macro blocks per warp: +1 per wave for the staging and the reduction, +1 for a cluster
+            // (its barriers and the exchange of partial sums cost about as much as a macro block), +1 for
+            // a ring (small copies stream slower than one copy per row).
+            const int64_t cost = waves * (per_warp + 1) + (S > 1 ? 1 : 0) + (ns > 0 ? 1 : 0);
             if (best_cost < 0 || cost < best_cost || (cost == best_cost && ctas > best_ctas)) {
-                best_cost = cost; best_kw = kw; best_s = (int)S; best_ctas = ctas;
+                best_cost = cost; best_kw = kw; best_s = (int)S; best_ctas = ctas; best_ns = (int)ns;
             }
         }
     }
     if (best_cost < 0) return -3;                                     // caller splits the tokens
     const int64_t kseg = ((nmacro + best_s - 1) / best_s) * 256;
-    switch (best_kw) {
-    case 1: return launch_gtc_kw<QT, NT, XBF16, 1>(wq, N, K, x, M, y, best_s, kseg, st);
-    case 2: return launch_gtc_kw<QT, NT, XBF16, 2>(wq, N, K, x, M, y, best_s, kseg, st);
-    case 4: return launch_gtc_kw<QT, NT, XBF16, 4>(wq, N, K, x, M, y, best_s, kseg, st);
-    default: return launch_gtc_kw<QT, NT, XBF16, 8>(wq, N, K, x, M, y, best_s, kseg, st);
-    }
+    if constexpr (KWMAX >= 8) if (best_kw == 8) return launch_gtc_kw<QT, NT, XBF16, 8>(wq, N, K, x, M, y, best_s, kseg, best_ns, status, st);
+    if constexpr (KWMAX >= 4) if (best_kw == 4) return launch_gtc_kw<QT, NT, XBF16, 4>(wq, N, K, x, M, y, best_s, kseg, best_ns, status, st);
+    if constexpr (KWMAX >= 2) if (best_kw == 2) return launch_gtc_kw<QT, NT, XBF16, 2>(wq, N, K, x, M, y, best_s, kseg, best_ns, status, st);
+    return launch_gtc_kw<QT, NT, XBF16, 1>(wq, N, K, x, M, y, best_s, kseg, best_ns, status, st);
 }
 
 struct GtcLaunch {
@@ -764,16 +939,17 @@ struct GtcLaunch {
     const void *x;
     int M;
     float *y;
+    unsigned int *status;
     cudaStream_t st;
     template <int QT> int operator()() {
         if constexpr (QT <= T_BF16) {
             return -1;
         } else {
-            if (xbf16) return M <= 8 ? launch_gtc_t<QT, 1, true>(wq, N, K, x, M, y, st)
-                                     : launch_gtc_t<QT, 2, true>(wq, N, K, x, M, y, st);
-            if (M <= 4) return launch_gtc_t<QT, 1, false>(wq, N, K, x, M, y, st);
-            if (M <= 8) return launch_gtc_t<QT, 2, false>(wq, N, K, x, M, y, st);
-            return launch_gtc_t<QT, 4, false>(wq, N, K, x, M, y, st);
+            if (xbf16) return M <= 8 ? launch_gtc_t<QT, 1, true>(wq, N, K, x, M, y, status, st)
+                                     : launch_gtc_t<QT, 2, true>(wq, N, K, x, M, y, status, st);
+            if (M <= 4) return launch_gtc_t<QT, 1, false>(wq, N, K, x, M, y, status, st);
+            if (M <= 8) return launch_gtc_t<QT, 2, false>(wq, N, K, x, M, y, status, st);
+            return launch_gtc_t<QT, 4, false>(wq, N, K, x, M, y, status, st);
         }
     }
 };
@@ -783,9 +959,10 @@ struct GtcLaunch {
 // M <= 16 tokens (bigger M is split into groups of 16 by the caller). Returns -3 when the K segments a
 // cluster allows cannot hold the activations of this many tokens (the caller then halves the group).
 int launch_gemv_tc(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int M, float *y,
-                   cudaStream_t st) {
-    GtcLaunch f{xbf16, wq, N, K, x, M, y, st};
+                   unsigned int *status, cudaStream_t st) {
+    GtcLaunch f{xbf16, wq, N, K, x, M, y, status, st};
     return dispatch_type(qt, f);
 }
 
 }  // namespace wqk
+

@@ -13,7 +13,7 @@ __device__ unsigned int g_status = 0;
 int launch_gemv(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int64_t M, float *y,
                 cudaStream_t st);
 int launch_gemv_tc(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int M, float *y,
-                   cudaStream_t st);
+                   unsigned int *status, cudaStream_t st);
 int launch_mm(int qt, int tile, const void *wq, int64_t N, int64_t K, const void *x_bf16, int64_t M, float *y,
               float *part, unsigned int *status, cudaStream_t st);
 size_t mm_partial_bytes(int64_t N, int64_t K, int64_t M);
@@ -69,12 +69,14 @@ int run_matvec(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const v
                cudaStream_t st) {
     if (is_plain(qt)) return launch_gemv(qt, xbf16, wq, N, K, x, M, y, st);
     const int esz = xbf16 ? 2 : 4;
+    unsigned int *status = status_ptr();
+    if (!status) return QMM_ECUDA;
     for (int64_t m0 = 0; m0 < M;) {
         int mg = (int)((M - m0) < 16 ? (M - m0) : 16);
         int rc;
         for (;;) {
             rc = launch_gemv_tc(qt, xbf16, wq, N, K, static_cast<const uint8_t *>(x) + m0 * K * esz, mg,
-                                y + m0 * N, st);
+                                y + m0 * N, status, st);
             if (rc != -3 || mg <= 4) break;
             mg = (mg + 1) / 2;
         }

@@ -915,10 +915,12 @@ int launch_gtc_t(const void *wq, int64_t N, int64_t K, const void *x, int M, flo
             if constexpr (KWMAX >= 8) if (kw == 8) resident = gtc_capacity<QT, NT, XBF16, 8>(S, smem);
             if (resident <= 0) continue;
             const int64_t waves = (ctas + resident - 1) / resident;
-            // In macro blocks per warp: +1 per wave for the staging and the reduction, +1 for a cluster
-            // (its barriers and the exchange of partial sums cost about as much as a macro block), +1 for
-            // a ring (small copies stream slower than one copy per row).
-            const int64_t cost = waves * (per_warp + 1) + (S > 1 ? 1 : 0) + (ns > 0 ? 1 : 0);
+            // In macro blocks per warp: +2 per wave for its start, the activation staging and the
+            // reduction, +1 more per 4096 activations a CTA stages, +1 for a cluster (its barriers and the
+            // exchange of partial sums cost about as much as a macro block), +1 for a ring (small copies
+            // stream slower than one copy per row).
+            const int64_t cost = waves * (per_warp + 2) + ((int64_t)M * kseg) / 4096 + (S > 1 ? 1 : 0) +
+                                 (ns > 0 ? 1 : 0);
             if (best_cost < 0 || cost < best_cost || (cost == best_cost && ctas > best_ctas)) {
                 best_cost = cost; best_kw = kw; best_s = (int)S; best_ctas = ctas; best_ns = (int)ns;
             }

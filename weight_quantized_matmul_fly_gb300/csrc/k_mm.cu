@@ -5,7 +5,8 @@
 // reads those rows' quantized blocks, dequantizes them into shared memory and multiplies them by every
 // token it holds, so each weight is fetched and dequantized once per token tile. Here:
 //   - a CTA owns BM = 128 weight rows (the MMA's M) and J token tiles of T = 32, 64 or 128 tokens (the
-//     MMA's N), J*T <= 256; the J tiles share every decoded slab;
+//     MMA's N), J*T <= 256, or 512 for large M (the whole tensor memory); the J tiles share every decoded
+//     slab, so a larger J*T divides the decoding work per multiply-add;
 //   - warp 0 loads the J*T x 64 bf16 activation tile of each K step by TMA (rows past M read as zero);
 //   - warps 2..9 decode the 128 x 64 weight slab of each step to bf16 (round to nearest even of the
 //     binary32 value) straight into the 128-byte-swizzled K-major layout tcgen05 reads;
@@ -27,14 +28,17 @@ namespace mm {
 
 constexpr int BM = 128;            // weight rows per CTA
 constexpr int BK = 64;             // columns per K step: one 128-byte swizzle row of bf16
-constexpr int STAGES = 4;
+constexpr int MAX_STAGES = 4;
 constexpr int A_STAGE = BM * BK * 2;   // 16 KB
 constexpr int NDEC = 8;                // decoder / epilogue warps
 constexpr int THREADS = 32 * (2 + NDEC);
 
 __host__ __device__ constexpr int b_stage_bytes(int TN) { return TN * BK * 2; }
+// Operand stages: four up to 256 tokens per CTA; two at 512 (80 KB each). At 512 tokens one K step of MMAs
+// takes about twice as long as decoding the step's weights, so two stages keep the tensor core fed.
+__host__ __device__ constexpr int stages_of(int TN) { return TN > 256 ? 2 : 4; }
 __host__ __device__ constexpr int smem_bytes(int TN) {
-    return 1024 /* alignment slack */ + STAGES * (A_STAGE + b_stage_bytes(TN)) + 256 /* barriers */;
+    return 1024 /* alignment slack */ + stages_of(TN) * (A_STAGE + b_stage_bytes(TN)) + 256 /* barriers */;
 }
 
 // Byte offset of the 16-byte piece p (bf16 columns 8p .. 8p+7) of row r in a 128-byte-swizzled tile.
@@ -191,7 +195,7 @@ template <> struct Slab<T_Q4_0> {
 };
 
 struct Smem {
-    uint64_t full_b[STAGES], full_a[STAGES], empty[STAGES], done;
+    uint64_t full_b[MAX_STAGES], full_a[MAX_STAGES], empty[MAX_STAGES], done;
     uint32_t tmem;
     int abort;
 };
@@ -203,7 +207,8 @@ __global__ void __launch_bounds__(THREADS, 1)
               int64_t rowbytes, int M, float *__restrict__ out, int64_t split_stride, int ksteps_per_split,
               unsigned int *status) {
     constexpr int TN = T * J;
-    constexpr uint32_t TMEM_COLS = TN <= 32 ? 32 : (TN <= 64 ? 64 : (TN <= 128 ? 128 : 256));
+    constexpr int STAGES = stages_of(TN);
+    constexpr uint32_t TMEM_COLS = TN <= 32 ? 32 : (TN <= 64 ? 64 : (TN <= 128 ? 128 : (TN <= 256 ? 256 : 512)));
     constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, T);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -251,7 +256,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 if (*(volatile int *)&sm->abort) break;
                 ptx::mbar_arrive_expect_tx(&sm->full_b[s], (uint32_t)b_stage_bytes(TN));
-                ptx::tma_load_2d(sB + s * b_stage_bytes(TN), &tmap_x, (kbeg + i) * BK, m0, &sm->full_b[s]);
+                // a tensor-map box has at most 256 rows: 512 tokens take two boxes
+#pragma unroll
+                for (int q = 0; q < (TN > 256 ? TN / 256 : 1); ++q)
+                    ptx::tma_load_2d(sB + s * b_stage_bytes(TN) + q * 256 * 128, &tmap_x, (kbeg + i) * BK,
+                                     m0 + 256 * q, &sm->full_b[s]);
                 issued = i + 1;
             }
             // every requested tile lands before the CTA may exit
@@ -440,8 +449,19 @@ static bool make_x_tmap(CUtensorMap *map, const void *xb, int64_t M, int64_t K, 
 namespace {
 
 // Token tiles per CTA: as many as fit 256 columns, but not more than the tokens need (a power of two).
-inline int tiles_per_cta(int T, int64_t M) {
-    int j = 256 / T;
+// 512 columns (T >= 64) when the CTAs of 512 tokens, times the K split, still fill every SM: each weight
+// slab is then decoded once per 512 tokens instead of 256.
+inline int tiles_per_cta(int T, int64_t N, int64_t M, int S) {
+    static int nsm = 0;
+    if (!nsm) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0)
+            nsm = 148;
+    }
+    const int64_t rowblocks = (N + mm::BM - 1) / mm::BM;
+    const bool wide = T >= 64 && rowblocks * ((M + 511) / 512) * S >= nsm;
+    int j = (wide ? 512 : 256) / T;
     const int64_t need = (M + T - 1) / T;
     while (j > 1 && j / 2 >= need) j /= 2;
     return j;
@@ -451,7 +471,7 @@ template <int QT, int T, int J>
 int launch_mm_t(const void *wq, int64_t N, int64_t K, const void *xb, int64_t M, float *out, int S, int kps,
                 int64_t split_stride, unsigned int *status, cudaStream_t st) {
     CUtensorMap map;
-    if (!make_x_tmap(&map, xb, M, K, T * J)) return -6;
+    if (!make_x_tmap(&map, xb, M, K, T * J > 256 ? 256 : T * J)) return -6;
     auto kern = mm::mm_kernel<QT, T, J>;
     const int smem = mm::smem_bytes(T * J);
     static bool attr_set = false;   // once per kernel instance
@@ -477,7 +497,8 @@ struct MmLaunch {
     unsigned int *status;
     cudaStream_t st;
     template <int QT, int T, int JJ> int go_j() {
-        if constexpr (T * JJ <= 256) return launch_mm_t<QT, T, JJ>(wq, N, K, xb, M, out, S, kps, split_stride, status, st);
+        if constexpr (T * JJ <= 256 || (T >= 64 && T * JJ <= 512))
+            return launch_mm_t<QT, T, JJ>(wq, N, K, xb, M, out, S, kps, split_stride, status, st);
         else return -7;
     }
     template <int QT, int T> int go() {
@@ -550,7 +571,7 @@ int launch_mm(int qt, int tile, const void *wq, int64_t N, int64_t K, const void
     const int kps = (int)((ksteps + S - 1) / S);
     float *out = S > 1 ? part : y;
     const int64_t sstride = split_stride_of(M, N);
-    MmLaunch f{tile, tiles_per_cta(tile, M), wq, N, K, x_bf16, M, out, S, kps, sstride, status, st};
+    MmLaunch f{tile, tiles_per_cta(tile, N, M, S), wq, N, K, x_bf16, M, out, S, kps, sstride, status, st};
     int rc = dispatch_type(qt, f);
     if (rc || S == 1) return rc;
     const int64_t n = M * N, n4 = n / 4;

@@ -23,6 +23,11 @@
  *     error nothing is launched. Arguments are checked on the host without dereferencing device memory.
  *   - wq, x and y must be 16-byte aligned.
  *   - Nothing here is thread-safe against concurrent calls that share an output buffer.
+ *   - The matmul kernels are launched with programmatic dependent launch: each may start while the
+ *     previous kernel in the stream finishes, and reads its WEIGHTS (wq) before waiting for it (x is read
+ *     and y written only after). So the kernel launched immediately before qmm / qmm_ws / qmm_noalloc /
+ *     qmm_id / qmm_with_tile on the same stream must not write wq; put any other kernel launch, a memory
+ *     copy or an event wait in between. qmm_quantize and qmm_dequant end with such a launch already.
  */
 #ifndef QMM_H
 #define QMM_H

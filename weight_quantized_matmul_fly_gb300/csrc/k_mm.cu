@@ -244,8 +244,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = sm->tmem;
 
+    // Programmatic dependent launch: the next kernel in the stream may start its prologue now; it waits
+    // for this grid's completion before touching memory this grid writes.
+    asm volatile("griddepcontrol.launch_dependents;");
     if (warp == 0) {
-        // ---------------- activation producer
+        // ---------------- activation producer: the activations may come from the preceding kernel, so
+        // they are loaded only after it has completed (the weights, which no kernel here writes, are
+        // decoded meanwhile)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         if (lane == 0) {
             int issued = 0;
             for (int i = 0; i < nsteps; ++i) {
@@ -348,7 +354,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 r1 = r2;
             }
         }
-        // ---------------- epilogue: TMEM lanes = weight rows, columns = tokens
+        // ---------------- epilogue: TMEM lanes = weight rows, columns = tokens (written only once the
+        // preceding kernel has completed)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
         const int half = (warp - 2) >> 2;       // two warps per quarter split the columns
         const int r = n0 + 32 * q + lane;
@@ -387,6 +395,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 // y[i] = sum over s of part[s][i], s ascending (deterministic K-split reduction).
 __global__ void splitk_reduce_kernel(const float4 *__restrict__ part, int64_t stride4, int S, float4 *__restrict__ y,
                                      int64_t n4) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
         float4 a = part[i];
         for (int s = 1; s < S; ++s) {
@@ -398,6 +408,8 @@ __global__ void splitk_reduce_kernel(const float4 *__restrict__ part, int64_t st
 }
 __global__ void splitk_reduce_tail_kernel(const float *__restrict__ part, int64_t stride, int S, float *__restrict__ y,
                                           int64_t beg, int64_t n) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     for (int64_t i = beg + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         float a = part[i];
         for (int s = 1; s < S; ++s) a += part[i + s * stride];
@@ -407,6 +419,8 @@ __global__ void splitk_reduce_tail_kernel(const float *__restrict__ part, int64_
 
 // binary32 -> bfloat16 (round to nearest even), 8 elements per thread; n is a multiple of 8.
 __global__ void x_to_bf16_kernel(const float4 *__restrict__ x, uint4 *__restrict__ out, int64_t n8) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
         const float4 a = x[2 * i], b = x[2 * i + 1];
         out[i] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
@@ -448,6 +462,24 @@ static bool make_x_tmap(CUtensorMap *map, const void *xb, int64_t M, int64_t K, 
 
 namespace {
 
+// Launch with programmatic stream serialization: the kernel may start while its predecessor in the stream
+// finishes; it orders its own memory accesses with griddepcontrol.wait. Returns 0 or -6.
+template <typename... Args>
+int launch_pdl(const void *kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *argv[] = {reinterpret_cast<void *>(&args)...};
+    return cudaLaunchKernelExC(&cfg, kern, argv) == cudaSuccess ? 0 : -6;
+}
+
 // Token tiles per CTA: as many as fit 256 columns, but not more than the tokens need (a power of two).
 // 512 columns (T >= 64) when the CTAs of 512 tokens, times the K split, still fill every SM: each weight
 // slab is then decoded once per 512 tokens instead of 256.
@@ -480,9 +512,11 @@ int launch_mm_t(const void *wq, int64_t N, int64_t K, const void *xb, int64_t M,
         attr_set = true;
     }
     dim3 grid((unsigned)((N + mm::BM - 1) / mm::BM), (unsigned)((M + T * J - 1) / (T * J)), (unsigned)S);
-    kern<<<grid, mm::THREADS, smem, st>>>(map, static_cast<const uint8_t *>(wq), (int)N, K, row_bytes(QT, K),
-                                          (int)M, out, split_stride, kps, status);
-    return cudaGetLastError() == cudaSuccess ? 0 : -6;
+    const int64_t rb = row_bytes(QT, K);
+    const uint8_t *w8 = static_cast<const uint8_t *>(wq);
+    const int Ni = (int)N, Mi = (int)M;
+    return launch_pdl(reinterpret_cast<const void *>(kern), grid, dim3(mm::THREADS), (size_t)smem, st, map, w8, Ni, K,
+                      rb, Mi, out, split_stride, kps, status);
 }
 
 struct MmLaunch {
@@ -578,11 +612,21 @@ int launch_mm(int qt, int tile, const void *wq, int64_t N, int64_t K, const void
     if (n4 > 0) {
         int64_t blocks = (n4 + 255) / 256;
         if (blocks > 152 * 8) blocks = 152 * 8;
-        mm::splitk_reduce_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<const float4 *>(part),
-                                                                   sstride / 4, S, reinterpret_cast<float4 *>(y), n4);
+        const float4 *p4 = reinterpret_cast<const float4 *>(part);
+        float4 *y4 = reinterpret_cast<float4 *>(y);
+        const int64_t s4 = sstride / 4;
+        if (launch_pdl(reinterpret_cast<const void *>(mm::splitk_reduce_kernel), dim3((unsigned)blocks), dim3(256), 0,
+                       st, p4, s4, S, y4, n4))
+            return -6;
     }
-    if (n % 4) mm::splitk_reduce_tail_kernel<<<1, 32, 0, st>>>(part, sstride, S, y, n4 * 4, n);
-    return cudaGetLastError() == cudaSuccess ? 0 : -6;
+    if (n % 4) {
+        const float *pc = part;
+        const int64_t beg = n4 * 4;
+        if (launch_pdl(reinterpret_cast<const void *>(mm::splitk_reduce_tail_kernel), dim3(1), dim3(32), 0, st, pc,
+                       sstride, S, y, beg, n))
+            return -6;
+    }
+    return 0;
 }
 
 int launch_x_to_bf16(const float *x, void *out, int64_t n, cudaStream_t st) {
@@ -591,9 +635,10 @@ int launch_x_to_bf16(const float *x, void *out, int64_t n, cudaStream_t st) {
     int64_t blocks = (n8 + threads - 1) / threads;
     if (blocks > 152 * 16) blocks = 152 * 16;
     if (blocks < 1) blocks = 1;
-    mm::x_to_bf16_kernel<<<(unsigned)blocks, threads, 0, st>>>(reinterpret_cast<const float4 *>(x),
-                                                               static_cast<uint4 *>(out), n8);
-    return cudaGetLastError() == cudaSuccess ? 0 : -6;
+    const float4 *x4 = reinterpret_cast<const float4 *>(x);
+    uint4 *o4 = static_cast<uint4 *>(out);
+    return launch_pdl(reinterpret_cast<const void *>(mm::x_to_bf16_kernel), dim3((unsigned)blocks), dim3(threads), 0,
+                      st, x4, o4, n8);
 }
 
 }  // namespace wqk

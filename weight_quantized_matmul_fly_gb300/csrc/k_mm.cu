@@ -6,7 +6,8 @@
 // token it holds, so each weight is fetched and dequantized once per token tile. Here:
 //   - a CTA owns BM = 128 weight rows (the MMA's M) and J token tiles of T = 32, 64 or 128 tokens (the
 //     MMA's N), J*T <= 256, or 512 for large M (the whole tensor memory); the J tiles share every decoded
-//     slab, so a larger J*T divides the decoding work per multiply-add;
+//     slab, so a larger J*T divides the decoding work per multiply-add (J = 1..6 or 8, only as many tiles
+//     as the tokens need);
 //   - warp 0 loads the J*T x 64 bf16 activation tile of each K step by TMA (rows past M read as zero);
 //   - warps 2..9 decode the 128 x 64 weight slab of each step to bf16 (round to nearest even of the
 //     binary32 value) straight into the 128-byte-swizzled K-major layout tcgen05 reads;
@@ -496,6 +497,9 @@ inline int tiles_per_cta(int T, int64_t N, int64_t M, int S) {
     int j = (wide ? 512 : 256) / T;
     const int64_t need = (M + T - 1) / T;
     while (j > 1 && j / 2 >= need) j /= 2;
+    // 3, 5 and 6 tiles too, so that a CTA does not multiply up to twice the tokens it holds
+    if (j == 4 && need == 3 && T <= 64) j = 3;
+    if (j == 8 && need <= 6 && need >= 5 && T == 32) j = (int)need;
     return j;
 }
 
@@ -531,7 +535,8 @@ struct MmLaunch {
     unsigned int *status;
     cudaStream_t st;
     template <int QT, int T, int JJ> int go_j() {
-        if constexpr (T * JJ <= 256 || (T >= 64 && T * JJ <= 512))
+        if constexpr ((T * JJ <= 256 && ((JJ & (JJ - 1)) == 0 || T == 32 || (T == 64 && JJ == 3))) ||
+                      (T >= 64 && T * JJ <= 512 && (JJ & (JJ - 1)) == 0))
             return launch_mm_t<QT, T, JJ>(wq, N, K, xb, M, out, S, kps, split_stride, status, st);
         else return -7;
     }
@@ -539,7 +544,10 @@ struct MmLaunch {
         switch (J) {
         case 1: return go_j<QT, T, 1>();
         case 2: return go_j<QT, T, 2>();
+        case 3: return go_j<QT, T, 3>();
         case 4: return go_j<QT, T, 4>();
+        case 5: return go_j<QT, T, 5>();
+        case 6: return go_j<QT, T, 6>();
         case 8: return go_j<QT, T, 8>();
         default: return -7;
         }

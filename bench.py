@@ -43,6 +43,24 @@ WORKLOAD = ("Qwen3-Embedding-4B layer: attn_q 4096x2560 Q4_K, attn_k 1024x2560 Q
             "weights N(0,0.02) quantized")
 
 
+# DRAM traffic per launch of the dominant kernel, from one ncu capture of the bench's own step (see
+# profiles/mm_kernel_qwen3_emb_4b_layer_m512_m2048.md): dram__bytes_read.sum + dram__bytes_write.sum averaged
+# over the 14 mm_kernel launches with M in {512, 2048}. Valid only for the kernel source it was taken on.
+MM_TRAFFIC = {"bytes_per_launch": 21.90e6, "launches": 14,
+              "source": "weight_quantized_matmul_fly_gb300/csrc/k_mm.cu",
+              "sha256": "0e77186df706d7f78434e8d2b01874faf4370a3483a483114df1734f7fd7c156"}
+
+
+def mm_traffic():
+    """The recorded traffic per launch, or None when the kernel source changed since it was measured."""
+    import hashlib
+    try:
+        h = hashlib.sha256(open(os.path.join(ROOT, MM_TRAFFIC["source"]), "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return MM_TRAFFIC["bytes_per_launch"] if h == MM_TRAFFIC["sha256"] else None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -280,7 +298,8 @@ def run_ours(args):
         roof = {"bound": "tensor", "kernel": "mm_kernel (tcgen05) incl. its bf16 activation pre-pass",
                 "calls": "M in {512, 2048}", "achieved": round(ach, 2), "peak": peaks["bf16_tflops_sustained"],
                 "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops_sustained"], 4),
-                "peak_kind": "bf16 sustained, %s" % peaks["source"], "traffic": None,
+                "peak_kind": "bf16 sustained, %s" % peaks["source"], "traffic": mm_traffic(),
+                "traffic_unit": "DRAM bytes per mm_kernel launch (ncu, same calls)",
                 "algorithmic_per_launch": "2*M*N*K flops"}
     else:
         ach = wb_small / t_small / 1e9

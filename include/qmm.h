@@ -163,8 +163,9 @@ int qmm_pick_tile(int64_t M);
 /* Which path qmm() takes for M tokens: 0 = mat-vec, 32/64/128 = tensor-core tile. */
 int qmm_pick_path(int qtype, int64_t N, int64_t K, int64_t M);
 
-/* How many kernels one qmm() / qmm_ws() call with these arguments launches (diagnostic; the mat-vec path
- * may launch more when its activations have to be processed in smaller token groups). */
+/* How many kernels one qmm() / qmm_ws() call with these arguments launches (diagnostic). The mat-vec path
+ * is planned as the call would plan it (token groups of 16, halved where their activations do not fit on
+ * chip), which needs the current device; without one it assumes one launch per 16 tokens. */
 int qmm_launch_count(int qtype, int64_t N, int64_t K, int64_t M);
 
 /*

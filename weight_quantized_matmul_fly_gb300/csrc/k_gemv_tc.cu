@@ -876,7 +876,7 @@ int launch_gtc_kw(const void *wq, int64_t N, int64_t K, const void *x, int M, fl
 // warp's ring takes as many stages as the shared memory left over allows (at most its macro blocks).
 template <int QT, int NT, bool XBF16>
 int launch_gtc_t(const void *wq, int64_t N, int64_t K, const void *x, int M, float *y, unsigned int *status,
-                 cudaStream_t st) {
+                 cudaStream_t st, bool dry) {
     using LY = gtc::Layout<NT, XBF16>;
     constexpr int UNIT = gtc::Frag<QT>::UNIT, SLOT = gtc::slot_bytes<QT>();
     constexpr int MB_BYTES = 256 / TypeInfo<QT>::QK * TypeInfo<QT>::BYTES;   // bytes of a macro block
@@ -927,6 +927,7 @@ int launch_gtc_t(const void *wq, int64_t N, int64_t K, const void *x, int M, flo
         }
     }
     if (best_cost < 0) return -3;                                     // caller splits the tokens
+    if (dry) return 0;                                                // planning only (launch counting)
     const int64_t kseg = ((nmacro + best_s - 1) / best_s) * 256;
     if constexpr (KWMAX >= 8) if (best_kw == 8) return launch_gtc_kw<QT, NT, XBF16, 8>(wq, N, K, x, M, y, best_s, kseg, best_ns, status, st);
     if constexpr (KWMAX >= 4) if (best_kw == 4) return launch_gtc_kw<QT, NT, XBF16, 4>(wq, N, K, x, M, y, best_s, kseg, best_ns, status, st);
@@ -943,15 +944,16 @@ struct GtcLaunch {
     float *y;
     unsigned int *status;
     cudaStream_t st;
+    bool dry;
     template <int QT> int operator()() {
         if constexpr (QT <= T_BF16) {
             return -1;
         } else {
-            if (xbf16) return M <= 8 ? launch_gtc_t<QT, 1, true>(wq, N, K, x, M, y, status, st)
-                                     : launch_gtc_t<QT, 2, true>(wq, N, K, x, M, y, status, st);
-            if (M <= 4) return launch_gtc_t<QT, 1, false>(wq, N, K, x, M, y, status, st);
-            if (M <= 8) return launch_gtc_t<QT, 2, false>(wq, N, K, x, M, y, status, st);
-            return launch_gtc_t<QT, 4, false>(wq, N, K, x, M, y, status, st);
+            if (xbf16) return M <= 8 ? launch_gtc_t<QT, 1, true>(wq, N, K, x, M, y, status, st, dry)
+                                     : launch_gtc_t<QT, 2, true>(wq, N, K, x, M, y, status, st, dry);
+            if (M <= 4) return launch_gtc_t<QT, 1, false>(wq, N, K, x, M, y, status, st, dry);
+            if (M <= 8) return launch_gtc_t<QT, 2, false>(wq, N, K, x, M, y, status, st, dry);
+            return launch_gtc_t<QT, 4, false>(wq, N, K, x, M, y, status, st, dry);
         }
     }
 };
@@ -960,9 +962,10 @@ struct GtcLaunch {
 
 // M <= 16 tokens (bigger M is split into groups of 16 by the caller). Returns -3 when the K segments a
 // cluster allows cannot hold the activations of this many tokens (the caller then halves the group).
+// dry: plan only, launch nothing (0 or -3), for counting launches.
 int launch_gemv_tc(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int M, float *y,
-                   unsigned int *status, cudaStream_t st) {
-    GtcLaunch f{xbf16, wq, N, K, x, M, y, status, st};
+                   unsigned int *status, cudaStream_t st, bool dry) {
+    GtcLaunch f{xbf16, wq, N, K, x, M, y, status, st, dry};
     return dispatch_type(qt, f);
 }
 

@@ -13,7 +13,7 @@ __device__ unsigned int g_status = 0;
 int launch_gemv(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int64_t M, float *y,
                 cudaStream_t st);
 int launch_gemv_tc(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int M, float *y,
-                   unsigned int *status, cudaStream_t st);
+                   unsigned int *status, cudaStream_t st, bool dry = false);
 int launch_mm(int qt, int tile, const void *wq, int64_t N, int64_t K, const void *x_bf16, int64_t M, float *y,
               float *part, unsigned int *status, cudaStream_t st);
 size_t mm_partial_bytes(int64_t N, int64_t K, int64_t M);
@@ -65,24 +65,31 @@ unsigned int *status_ptr() {
 
 // The mat-vec path: quantized types on the tensor-core mat-vec kernel (16 tokens per launch at most,
 // halved when the activations of a K segment would not fit on chip); the plain types on the binary32 one.
+// With `launches` non-null nothing is launched: the launches the call would make are counted instead.
 int run_matvec(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int64_t M, float *y,
-               cudaStream_t st) {
-    if (is_plain(qt)) return launch_gemv(qt, xbf16, wq, N, K, x, M, y, st);
+               cudaStream_t st, int *launches = nullptr) {
+    if (is_plain(qt)) {
+        if (launches) { *launches = (int)((M + 15) / 16); return 0; }
+        return launch_gemv(qt, xbf16, wq, N, K, x, M, y, st);
+    }
     const int esz = xbf16 ? 2 : 4;
-    unsigned int *status = status_ptr();
-    if (!status) return QMM_ECUDA;
+    unsigned int *status = launches ? nullptr : status_ptr();
+    if (!launches && !status) return QMM_ECUDA;
+    int count = 0;
     for (int64_t m0 = 0; m0 < M;) {
         int mg = (int)((M - m0) < 16 ? (M - m0) : 16);
         int rc;
         for (;;) {
             rc = launch_gemv_tc(qt, xbf16, wq, N, K, static_cast<const uint8_t *>(x) + m0 * K * esz, mg,
-                                y + m0 * N, status, st);
+                                y + m0 * N, status, st, launches != nullptr);
             if (rc != -3 || mg <= 4) break;
             mg = (mg + 1) / 2;
         }
         if (rc) return rc == -3 ? QMM_EDIM : rc;
+        ++count;
         m0 += mg;
     }
+    if (launches) *launches = count;
     return 0;
 }
 
@@ -250,8 +257,12 @@ int qmm_launch_count(int qtype, int64_t N, int64_t K, int64_t M) {
     const int path = qmm_pick_path(qtype, N, K, M);
     if (path < 0) return path;
     if (path == 0) {
-        // binary32 mat-vec for the plain types (16 tokens per launch), tensor-core mat-vec for the others
-        return (int)((M + 15) / 16);
+        // the mat-vec path's own plan (token groups of 16, halved where the activations would not fit)
+        // (one launch per 16 tokens when there is no device to plan on)
+        int n = 0;
+        const int rc = run_matvec(qtype & 0xff, (qtype & QMM_X_BF16) != 0, nullptr, N, K, nullptr, M, nullptr,
+                                  nullptr, &n);
+        return rc ? (int)((M + 15) / 16) : n;
     }
     const int S = mm_ksplit(N, K, M);
     return ((qtype & QMM_X_BF16) ? 0 : 1) + 1 + (S > 1 ? 1 + ((M * N) % 4 ? 1 : 0) : 0);

@@ -9,10 +9,13 @@
 //     slab, so a larger J*T divides the decoding work per multiply-add (J = 1..6 or 8, only as many tiles
 //     as the tokens need);
 //   - warp 0 loads the J*T x 64 bf16 activation tile of each K step by TMA (rows past M read as zero);
-//   - warps 2..9 decode the 128 x 64 weight slab of each step to bf16 (round to nearest even of the
-//     binary32 value) straight into the 128-byte-swizzled K-major layout tcgen05 reads;
-//   - warp 1 issues, per step, 4 (K = 16) x J tcgen05.mma into TMEM and commits them to the stage's
-//     "empty" barrier, which hands the stage back to the producer and the decoders;
+//   - warps 2..17 decode the 128 x 64 weight slab of each step to bf16 (round to nearest even of the
+//     binary32 value) straight into the 128-byte-swizzled K-major layout tcgen05 reads; they form two
+//     groups of 8 that take alternate K steps, so each keeps the raw bytes of its next two steps (four K
+//     steps ahead) in flight and twice as many warps hide the load latency;
+//   - warp 1 issues, per step, 4 (K = 16) tcgen05.mma of N = min(J*T, 256) tokens (two at 512) into TMEM
+//     and commits them to the stage's "empty" barrier, which hands the stage back to the producer and the
+//     decoders;
 //   - the decoder warps then read TMEM with tcgen05.ld and write y (or, when K is split over CTAs, a
 //     binary32 partial that a second kernel adds up in a fixed order).
 // Bit-identity across T: every output element sees the same K steps, the same K=16 MMAs in the same
@@ -31,7 +34,8 @@ constexpr int BM = 128;            // weight rows per CTA
 constexpr int BK = 64;             // columns per K step: one 128-byte swizzle row of bf16
 constexpr int MAX_STAGES = 4;
 constexpr int A_STAGE = BM * BK * 2;   // 16 KB
-constexpr int NDEC = 8;                // decoder / epilogue warps
+constexpr int NDEC = 16;               // decoder / epilogue warps: two groups of 8 taking alternate K steps
+constexpr int NGRP = NDEC / 8;         // decoder groups (one slab = 8 warps x 16 rows)
 constexpr int THREADS = 32 * (2 + NDEC);
 
 __host__ __device__ constexpr int b_stage_bytes(int TN) { return TN * BK * 2; }
@@ -210,7 +214,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int TN = T * J;
     constexpr int STAGES = stages_of(TN);
     constexpr uint32_t TMEM_COLS = TN <= 32 ? 32 : (TN <= 64 ? 64 : (TN <= 128 ? 128 : (TN <= 256 ? 256 : 512)));
-    constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, T);
+    // One MMA covers up to 256 token columns (all J tiles of T at once; the tiles are contiguous in
+    // shared memory and in TMEM): N = MN per instruction, NMMA instructions per K = 16.
+    constexpr int MN = TN > 256 ? 256 : TN, NMMA = TN / MN;
+    static_assert(MN % 16 == 0 && TN % MN == 0, "MMA N");
+    constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, MN);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *sA = smem;
@@ -229,7 +237,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(&sm->full_b[s], 1);
-            ptx::mbar_init(&sm->full_a[s], NDEC);
+            ptx::mbar_init(&sm->full_a[s], 8);   // the 8 warps of the group that decodes this step
             ptx::mbar_init(&sm->empty[s], 1);
         }
         ptx::mbar_init(&sm->done, 1);
@@ -290,10 +298,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
 #pragma unroll
-                    for (int jj = 0; jj < J; ++jj) {
-                        const uint64_t bdesc = ptx::sw128_desc(sB_u32 + s * b_stage_bytes(TN) + jj * T * 128);
+                    for (int jj = 0; jj < NMMA; ++jj) {
+                        const uint64_t bdesc = ptx::sw128_desc(sB_u32 + s * b_stage_bytes(TN) + jj * MN * 128);
                         // advancing 16 bf16 = 32 bytes inside the swizzle row moves the start address by 2 units
-                        ptx::mma_bf16(tmem + jj * T, adesc + 2 * kk, bdesc + 2 * kk, IDESC, (i | kk) != 0);
+                        ptx::mma_bf16(tmem + jj * MN, adesc + 2 * kk, bdesc + 2 * kk, IDESC, (i | kk) != 0);
                     }
                 }
                 ptx::mma_commit(&sm->empty[s]);
@@ -301,27 +309,29 @@ __global__ void __launch_bounds__(THREADS, 1)
             ptx::mma_commit(&sm->done);   // tracks every MMA issued above
         }
     } else {
-        // ---------------- decoders: warp d handles rows 16d .. 16d+15 of the slab; lane -> (row, chunk)
+        // ---------------- decoders: group grp decodes the K steps i = grp (mod NGRP); within a group warp
+        // dw handles rows 16dw .. 16dw+15 of the slab; lane -> (row, chunk)
         const int d = warp - 2;
-        const int r_local = 16 * d + (lane >> 1), h = lane & 1;
+        const int grp = d >> 3, dw = d & 7;
+        const int r_local = 16 * dw + (lane >> 1), h = lane & 1;
         const int row = n0 + r_local;
         const bool row_ok = row < N;
         const uint8_t *wrow = wq + (int64_t)(row_ok ? row : N - 1) * rowbytes;
         const int nchunks = (int)((K + 31) / 32);
         const uint32_t sA_u32 = ptx::smem_u32(sA);
         using SL = Slab<QT>;
-        // raw bytes of the next two K steps are in flight while a step is decoded
+        // raw bytes of the group's next two K steps are in flight while a step is decoded
         typename SL::Raw r0, r1, r2;
         if constexpr (SL::FAST) {
-            const int c0 = 2 * kbeg + h;
-            if (nsteps > 0 && c0 < nchunks) SL::load(r0, wrow, c0);
-            if (nsteps > 1 && c0 + 2 < nchunks) SL::load(r1, wrow, c0 + 2);
+            const int c0 = 2 * (kbeg + grp) + h;
+            if (grp < nsteps && c0 < nchunks) SL::load(r0, wrow, c0);
+            if (grp + NGRP < nsteps && c0 + 2 * NGRP < nchunks) SL::load(r1, wrow, c0 + 2 * NGRP);
         }
-        for (int i = 0; i < nsteps; ++i) {
+        for (int i = grp; i < nsteps; i += NGRP) {
             const int s = i % STAGES;
             const int c = 2 * (kbeg + i) + h;
             if constexpr (SL::FAST) {
-                if (i + 2 < nsteps && c + 4 < nchunks) SL::load(r2, wrow, c + 4);
+                if (i + 2 * NGRP < nsteps && c + 4 * NGRP < nchunks) SL::load(r2, wrow, c + 4 * NGRP);
             }
             if (i >= STAGES && !ptx::mbar_wait(&sm->empty[s], ((i / STAGES) - 1) & 1, status)) {
                 sm->abort = 1;
@@ -358,16 +368,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---------------- epilogue: TMEM lanes = weight rows, columns = tokens (written only once the
         // preceding kernel has completed)
         asm volatile("griddepcontrol.wait;" ::: "memory");
+        constexpr int PARTS = NDEC / 4;         // warps per TMEM lane quarter; they split the columns
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
-        const int half = (warp - 2) >> 2;       // two warps per quarter split the columns
+        const int part = (warp - 2) >> 2;       // (q, part) runs over all quarters x parts once
         const int r = n0 + 32 * q + lane;
         if (nsteps > 0) {
             const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(&sm->done, 0, status) && !*(volatile int *)&sm->abort);
             ptx::tc_fence_after();
             if (ok) {
                 const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
-#pragma unroll
-                for (int c0 = half * (TN / 2); c0 < (half + 1) * (TN / 2); c0 += 16) {
+                for (int c0 = 16 * part; c0 < TN; c0 += 16 * PARTS) {
                     uint32_t v[16];
                     ptx::tmem_ld_32x32b_x16(lane_base + c0, v);
                     ptx::tmem_ld_wait();
@@ -382,10 +392,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         } else {
             // an empty K split contributes zeros
-            for (int c0 = half * (TN / 2); c0 < (half + 1) * (TN / 2); ++c0) {
-                const int tok = m0 + c0;
-                if (r < N && tok < M) y[(int64_t)tok * N + r] = 0.0f;
-            }
+            for (int c0 = 16 * part; c0 < TN; c0 += 16 * PARTS)
+                for (int j = 0; j < 16; ++j) {
+                    const int tok = m0 + c0 + j;
+                    if (r < N && tok < M) y[(int64_t)tok * N + r] = 0.0f;
+                }
         }
     }
     ptx::tc_fence_before();

@@ -29,6 +29,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "../../include/qmm.h"
 #include "ptx.cuh"
 #include "qmm_common.cuh"
 
@@ -782,6 +783,283 @@ __global__ void __launch_bounds__(256, 2)
     }
 }
 
+
+// ------------------------------------------------------------------------------------------ expert-indexed
+// Expert-indexed mat-vec (the pages' MUL_MAT_ID; llama.cpp PR 28086, "metal : fix idle threads in
+// mul_mv_iq3_xxs for ne00 < 1024", "Overview"): y[(t*topk + j)*N + n] = sum_k dequant(W_e)[n, k] x[t, k]
+// with e = ids[t*topk + j]. CTA (row block, K segment, rank u) serves the u-th distinct expert in
+// ascending id order: it reads the routing table after waiting for its predecessor (the table usually
+// comes from the router kernel), copies that expert's rows of its row block into shared memory once (one
+// bulk copy per row, as the resident mode of the mat-vec kernel), and multiplies them by the activations
+// of every (token, slot) routed to the expert, TOK of them per pass, the activations gathered into MMA
+// columns. So each expert's weights are read once per call however many tokens chose it. CTAs whose rank
+// exceeds the number of distinct experts leave at once (the whole cluster, which shares the rank).
+struct IdExperts {
+    const uint8_t *p[QMM_MAX_EXPERTS];
+};
+
+template <int QT, int NT, bool XBF16, int KW>
+__global__ void __launch_bounds__(256, 2)
+    gemv_tc_id_kernel(const __grid_constant__ IdExperts ex, int E, int N, int64_t K, int64_t rowbytes,
+                      const void *__restrict__ x, const int32_t *__restrict__ ids, int M, int topk,
+                      float *__restrict__ y, int kseg, unsigned int *__restrict__ status) {
+    using F = Frag<QT>;
+    using LY = Layout<NT, XBF16>;
+    constexpr int WARPS = LY::WARPS, RG = WARPS / KW;
+    constexpr int UNIT = F::UNIT;
+    constexpr int TOK = LY::TOK;
+    constexpr int QK = TypeInfo<QT>::QK, BYTES = TypeInfo<QT>::BYTES;
+    constexpr int BPM = 256 / QK;
+    extern __shared__ __align__(16) uint8_t smem[];
+
+    const int S = gridDim.y;
+    const int u = blockIdx.z;
+    const int64_t kb = (int64_t)blockIdx.y * kseg;
+    const int64_t ke = (kb + kseg < K) ? kb + kseg : K;
+    const int kpad = kseg;
+    const int xst = LY::xs_stride(kpad), sxs = kpad / UNIT;
+    const int scols = LY::COLS;                        // all columns staged (the token count varies per pass)
+    const int nslot = M * topk;
+    const int rstride = resident_stride(kseg / 256 * BPM * BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    uint8_t *tile = smem + LY::BARS;
+    __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(tile + LY::tile_bytes(RG, kseg / 256 * BPM * BYTES));
+    float *sx = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(xs) + (size_t)scols * xst * 2);
+    float *part = sx + (size_t)TOK * sxs;              // [WARPS][16][TOK]
+    float *red = part + (size_t)WARPS * 16 * TOK;      // [S][RG*16*TOK] in rank 0
+    int *s_slot = reinterpret_cast<int *>(red + (S > 1 ? (size_t)S * RG * 16 * TOK : 0));   // [nslot]
+    unsigned char *s_used = reinterpret_cast<unsigned char *>(s_slot + nslot);              // [QMM_MAX_EXPERTS]
+    __shared__ int s_nexp, s_expert, s_ns;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const int rg = warp / KW, ks = warp % KW;
+    const int nrow0 = blockIdx.x * (16 * RG) + 16 * rg;
+
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    if (S > 1) cluster_arrive_relaxed();              // matched by the wait before the partials move
+
+    // ---- routing: distinct experts in ascending id order, and the slots routed to this CTA's expert.
+    //      The table is read once, into s_slot; the slot list of the expert later replaces it in place.
+    for (int i = tid; i < QMM_MAX_EXPERTS; i += WARPS * 32) s_used[i] = 0;
+    __syncthreads();
+    bool bad = false;
+    for (int i = tid; i < nslot; i += WARPS * 32) {
+        const int e = ids[i];
+        s_slot[i] = e;
+        if (e >= 0 && e < E) s_used[e] = 1;
+        else bad = true;
+    }
+    bad = __syncthreads_or(bad);
+    if (warp == 0) {
+        int base = 0, mine = -1;
+        for (int w0 = 0; w0 < QMM_MAX_EXPERTS; w0 += 32) {
+            const bool used = s_used[w0 + lane] != 0;
+            const unsigned b = __ballot_sync(0xffffffffu, used);
+            if (used && base + __popc(b & ((1u << lane) - 1u)) == u) mine = w0 + lane;
+            base += __popc(b);
+        }
+        mine = __reduce_max_sync(0xffffffffu, mine);
+        if (lane == 0) { s_nexp = base; s_expert = mine; }
+    }
+    __syncthreads();
+    if (bad && u == 0 && blockIdx.y == 0) {
+        // slots with an id outside [0, E): NaN rows (this CTA's rows) and a status bit
+        for (int p = 0; p < nslot; ++p) {
+            const int e = s_slot[p];
+            if (e < 0 || e >= E)
+                for (int r = tid; r < 16 * RG; r += WARPS * 32) {
+                    const int n = blockIdx.x * (16 * RG) + r;
+                    if (n < N) y[(int64_t)p * N + n] = __int_as_float(0x7fc00000);
+                }
+        }
+        if (tid == 0 && blockIdx.x == 0) atomicOr(status, kStatusBadId);
+    }
+    if (u >= s_nexp) {
+        if (S > 1) cluster_wait();                    // (the whole cluster leaves: it shares u)
+        return;
+    }
+    const int e = s_expert;
+    __syncthreads();                                  // the table in s_slot is read before it is compacted
+
+    // ---- this expert's rows of the row block, one bulk copy per row of the K segment (issued first)
+    const uint8_t *wq = ex.p[e];
+    const int64_t smb = kb / 256, nmb = (ke - kb + 255) / 256;
+    const int64_t mb_beg = smb + (nmb * ks) / KW, mb_end = smb + (nmb * (ks + 1)) / KW;
+    const int nsteps = (int)(mb_end - mb_beg);
+    const int64_t nblocks_row = K / QK;
+    const int64_t full_end = K / 256;
+    auto nblk_of = [&](int64_t mb) {
+        const int64_t r = nblocks_row - mb * BPM;
+        return (int)(r < BPM ? r : BPM);
+    };
+    uint64_t *gbar = bars + rg * NSMAX;
+    uint8_t *gtile = tile + (size_t)rg * 16 * rstride;
+    const uintptr_t wend = reinterpret_cast<uintptr_t>(wq) + (uintptr_t)N * (uintptr_t)rowbytes;
+    if (ks == 0) {
+        if (lane == 0) ptx::mbar_init(gbar, 16);
+        ptx::fence_mbar_init();
+        __syncwarp();
+        if (lane < 16) {
+            const int crow = nrow0 + lane < N ? nrow0 + lane : N - 1;
+            const uintptr_t a = reinterpret_cast<uintptr_t>(wq + (int64_t)crow * rowbytes + smb * BPM * BYTES);
+            const int64_t sblocks = (nblocks_row - smb * BPM) < (int64_t)(kseg / QK) ? nblocks_row - smb * BPM
+                                                                                     : (int64_t)(kseg / QK);
+            const uintptr_t en = a + (uintptr_t)sblocks * BYTES;
+            const uintptr_t a0 = a & ~(uintptr_t)15;
+            uintptr_t e1 = (en + 15) & ~(uintptr_t)15;
+            if (e1 > wend) e1 = wend & ~(uintptr_t)15;
+            uint8_t *dst = gtile + (size_t)lane * rstride;
+            for (uintptr_t q = e1 > a0 ? e1 : a0; q < en; ++q) dst[q - a0] = *reinterpret_cast<const uint8_t *>(q);
+            ptx::mbar_arrive_expect_tx(gbar, e1 > a0 ? (uint32_t)(e1 - a0) : 0u);
+            if (e1 > a0) ptx::bulk_load(dst, reinterpret_cast<const void *>(a0), (uint32_t)(e1 - a0), gbar);
+        }
+    }
+    if (warp == 0) {
+        // ordered compaction of the slots of expert e, in place: a chunk of 32 is read before any lane
+        // writes, and writes land at or before the chunk
+        int c = 0;
+        for (int p0 = 0; p0 < nslot; p0 += 32) {
+            const bool hit = p0 + lane < nslot && s_slot[p0 + lane] == e;
+            const unsigned b = __ballot_sync(0xffffffffu, hit);
+            if (hit) s_slot[c + __popc(b & ((1u << lane) - 1u))] = p0 + lane;
+            c += __popc(b);
+        }
+        if (lane == 0) s_ns = c;
+    }
+    __syncthreads();                                  // slot list and tile barrier initialised
+    const int ns = s_ns;
+    const uintptr_t radr0 = reinterpret_cast<uintptr_t>(wq + (int64_t)(nrow0 + g < N ? nrow0 + g : N - 1) * rowbytes);
+    const uintptr_t radr1 =
+        reinterpret_cast<uintptr_t>(wq + (int64_t)(nrow0 + g + 8 < N ? nrow0 + g + 8 : N - 1) * rowbytes);
+    const uintptr_t so = (uintptr_t)(smb * BPM * BYTES);
+    bool tile_ok = true;
+    if (S > 1) cluster_wait();                        // every CTA of the cluster has started
+
+    for (int p0 = 0; p0 < ns; p0 += TOK) {
+        const int mtok = ns - p0 < TOK ? ns - p0 : TOK;
+        // ---- gathered activations of this pass's tokens: bf16 columns and per-unit sums
+        {
+            const int k4n = kpad / 4;
+            const int total = mtok * k4n;             // a multiple of 64: warp-uniform loop
+            for (int idx = tid; idx < total; idx += WARPS * 32) {
+                const int tk = idx / k4n, k4 = idx - tk * k4n;
+                const int64_t k = kb + 4 * k4;
+                const int tok = s_slot[p0 + tk] / topk;
+                float v[4] = {0.f, 0.f, 0.f, 0.f};
+                if (k < ke) {
+                    if constexpr (XBF16) {
+                        const uint2 pv = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(x) +
+                                                                               (int64_t)tok * K + k));
+                        v[0] = __uint_as_float(pv.x << 16); v[1] = __uint_as_float(pv.x & 0xffff0000u);
+                        v[2] = __uint_as_float(pv.y << 16); v[3] = __uint_as_float(pv.y & 0xffff0000u);
+                    } else {
+                        const float4 pv = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(x) +
+                                                                                (int64_t)tok * K + k));
+                        v[0] = pv.x; v[1] = pv.y; v[2] = pv.z; v[3] = pv.w;
+                    }
+                }
+                if constexpr (XBF16) {
+                    __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]), h1 = __floats2bfloat162_rn(v[2], v[3]);
+                    *reinterpret_cast<uint2 *>(xs + (size_t)tk * xst + 4 * k4) =
+                        make_uint2(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1));
+                } else {
+                    float hi[4], lo[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        hi[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+                        lo[i] = __fsub_rn(v[i], hi[i]);
+                    }
+                    __nv_bfloat162 h0 = __floats2bfloat162_rn(hi[0], hi[1]), h1 = __floats2bfloat162_rn(hi[2], hi[3]);
+                    __nv_bfloat162 l0 = __floats2bfloat162_rn(lo[0], lo[1]), l1 = __floats2bfloat162_rn(lo[2], lo[3]);
+                    const int col = 8 * (tk >> 2) + 2 * (tk & 3);
+                    *reinterpret_cast<uint2 *>(xs + (size_t)col * xst + 4 * k4) =
+                        make_uint2(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1));
+                    *reinterpret_cast<uint2 *>(xs + (size_t)(col + 1) * xst + 4 * k4) =
+                        make_uint2(*reinterpret_cast<uint32_t *>(&l0), *reinterpret_cast<uint32_t *>(&l1));
+                }
+                float sum = (v[0] + v[1]) + (v[2] + v[3]);
+#pragma unroll
+                for (int off = 1; off < UNIT / 4; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                if ((k4 & (UNIT / 4 - 1)) == 0) sx[tk * sxs + (4 * k4) / UNIT] = sum;
+            }
+        }
+        __syncthreads();
+
+        float acc[NT][4];
+#pragma unroll
+        for (int mt = 0; mt < NT; ++mt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[mt][j] = 0.0f;
+        if (p0 == 0 && nsteps > 0)
+            tile_ok = __all_sync(0xffffffffu, ptx::mbar_wait(gbar, 0u, status));
+        if (tile_ok) {
+            typename F::Raw cur0, cur1;
+            for (int i = 0; i < nsteps; ++i) {
+                const int64_t mb = mb_beg + i;
+                const size_t jo = (size_t)(mb - smb) * BPM * BYTES;
+                F::load(cur0, gtile + (size_t)g * rstride + ((radr0 + so) & 15) + jo, t, nblk_of(mb));
+                F::load(cur1, gtile + (size_t)(g + 8) * rstride + ((radr1 + so) & 15) + jo, t, nblk_of(mb));
+                const int kloc = (int)(mb * 256 - kb);
+                if (mb < full_end)
+                    macro_step<QT, NT, XBF16, true>(cur0, cur1, xs, xst, sx, sxs, kloc, 16, g, t, scols - 1, acc);
+                else
+                    macro_step<QT, NT, XBF16, false>(cur0, cur1, xs, xst, sx, sxs, kloc, (int)((K - mb * 256) / 16), g,
+                                                     t, scols - 1, acc);
+            }
+        }
+        float *pw = part + (size_t)warp * 16 * TOK;
+#pragma unroll
+        for (int mt = 0; mt < NT; ++mt) {
+            if constexpr (XBF16) {
+                const int tk = 8 * mt + 2 * t;
+                pw[g * TOK + tk] = acc[mt][0]; pw[g * TOK + tk + 1] = acc[mt][1];
+                pw[(g + 8) * TOK + tk] = acc[mt][2]; pw[(g + 8) * TOK + tk + 1] = acc[mt][3];
+            } else {
+                const int tk = 4 * mt + t;
+                pw[g * TOK + tk] = acc[mt][0];
+                pw[(g + 8) * TOK + tk] = acc[mt][2];
+            }
+        }
+        __syncthreads();
+        // K slices (fixed order), then the K segments of the cluster in rank order (as the mat-vec kernel)
+        const int nres = RG * 16 * mtok;
+        const uint32_t rank = S > 1 ? cluster_rank() : 0;
+        const uint32_t red0 = S > 1 ? dsmem_addr(red, 0) : 0;
+        for (int idx = tid; idx < nres; idx += WARPS * 32) {
+            const int r = idx / mtok, tk = idx - r * mtok;
+            const int rgi = r >> 4, rr = r & 15;
+            float sum = 0.0f;
+#pragma unroll
+            for (int q = 0; q < KW; ++q) sum += part[((size_t)(rgi * KW + q) * 16 + rr) * TOK + tk];
+            if (S == 1) {
+                const int n = blockIdx.x * (16 * RG) + r;
+                if (n < N) y[(int64_t)s_slot[p0 + tk] * N + n] = sum;
+            } else {
+                st_dsmem_f32(red0 + 4u * (rank * (uint32_t)nres + (uint32_t)idx), sum);
+            }
+        }
+        if (S > 1) {
+            cluster_sync();
+            if (rank == 0) {
+                for (int idx = tid; idx < nres; idx += WARPS * 32) {
+                    const int r = idx / mtok, tk = idx - r * mtok;
+                    float sum = 0.0f;
+                    for (int q = 0; q < S; ++q) sum += red[q * nres + idx];
+                    const int n = blockIdx.x * (16 * RG) + r;
+                    if (n < N) y[(int64_t)s_slot[p0 + tk] * N + n] = sum;
+                }
+            }
+            cluster_sync();                           // rank 0 has read its slots before the next pass
+        }
+        __syncthreads();                              // activations and partials are reused by the next pass
+    }
+    // After a timeout nothing more is read from the tile, but the copies must land before the CTA exits.
+    if (!tile_ok) ptx::mbar_wait(gbar, 0u, status);
+    if (ns == 0 && nsteps > 0) ptx::mbar_wait(gbar, 0u, status);
+}
+
 }  // namespace gtc
 
 // ------------------------------------------------------------------------------------------ host side
@@ -958,6 +1236,114 @@ struct GtcLaunch {
     }
 };
 
+// ---- expert-indexed launches
+template <int QT, int NT, bool XBF16, int KW>
+int launch_gtc_id_kw(const gtc::IdExperts &ex, int E, int64_t N, int64_t K, const void *x, const int32_t *ids, int M,
+                     int topk, float *y, int S, int64_t kseg, size_t smem, unsigned int *status, cudaStream_t st) {
+    using LY = gtc::Layout<NT, XBF16>;
+    constexpr int RG = LY::WARPS / KW;
+    auto kern = gtc::gemv_tc_id_kernel<QT, NT, XBF16, KW>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap) != cudaSuccess)
+            return -6;
+        attr_set = true;
+    }
+    const int64_t dmax = (int64_t)M * topk < E ? (int64_t)M * topk : E;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((N + 16 * RG - 1) / (16 * RG)), (unsigned)S, (unsigned)dmax);
+    cfg.blockDim = dim3(LY::WARPS * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)S;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ex, E, (int)N, K, row_bytes(QT, K), x, ids, M, topk, y, (int)kseg,
+                                       status);
+    return e == cudaSuccess ? 0 : -6;
+}
+
+// Work split of the expert-indexed kernel: the per-expert matrices are narrow (K of a few macro blocks), so
+// the split takes the K slices per CTA and K segments per cluster (at most 4) that minimise waves x (macro
+// blocks per warp + a per-CTA prologue), over CTAs of every possible expert (those of absent experts leave
+// at once), with the whole row-block tile resident in shared memory. Returns -3 when no split fits.
+template <int QT, int NT, bool XBF16>
+int launch_gtc_id_t(const gtc::IdExperts &ex, int E, int64_t N, int64_t K, const void *x, const int32_t *ids, int M,
+                    int topk, float *y, unsigned int *status, cudaStream_t st) {
+    using LY = gtc::Layout<NT, XBF16>;
+    constexpr int UNIT = gtc::Frag<QT>::UNIT, TOK = LY::TOK;
+    constexpr int MB_BYTES = 256 / TypeInfo<QT>::QK * TypeInfo<QT>::BYTES;
+    constexpr int KWMAX = NT == 1 ? 8 : ((NT == 2 && !XBF16) ? 2 : 1);
+    const int64_t ngroups = (N + 15) / 16, nmacro = (K + 255) / 256;
+    const int nslot = M * topk;
+    const int64_t dmax = nslot < E ? nslot : E;
+    static int nsm = 0;
+    if (!nsm) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0)
+            nsm = 148;
+    }
+    int best_kw = 0, best_s = 1;
+    int64_t best_cost = -1;
+    size_t best_smem = 0;
+    for (int kw = 1; kw <= KWMAX; kw *= 2) {
+        if (kw > nmacro) break;
+        const int rg = 8 / kw;
+        const int64_t nrb = (ngroups + rg - 1) / rg;
+        for (int S = 1; S <= 4 && S <= nmacro; ++S) {
+            const int64_t kseg = ((nmacro + S - 1) / S) * 256;
+            if ((K + kseg - 1) / kseg != S) continue;
+            const size_t smem = LY::BARS + LY::tile_bytes(rg, (int)(kseg / 256 * MB_BYTES)) +
+                                LY::xbytes((int)kseg, UNIT, TOK) + LY::red_bytes(S, rg) +
+                                (((size_t)nslot * 4 + QMM_MAX_EXPERTS + 15) & ~(size_t)15);
+            if (smem > kSmemCap) continue;
+            const int64_t per_warp = (kseg / 256 + kw - 1) / kw;
+            // CTAs of every possible expert, two per SM; each wave also pays the routing prologue
+            const int64_t ctas = nrb * S * dmax;
+            const int64_t waves = (ctas + 2 * nsm - 1) / (2 * nsm);
+            const int64_t cost = 4 * waves * (per_warp + 3) + (S > 1 ? 4 : 0);
+            if (best_cost < 0 || cost < best_cost) {
+                best_cost = cost; best_kw = kw; best_s = S; best_smem = smem;
+            }
+        }
+    }
+    if (best_cost < 0) return -3;
+    const int64_t kseg = ((nmacro + best_s - 1) / best_s) * 256;
+    if constexpr (KWMAX >= 8) if (best_kw == 8) return launch_gtc_id_kw<QT, NT, XBF16, 8>(ex, E, N, K, x, ids, M, topk, y, best_s, kseg, best_smem, status, st);
+    if constexpr (KWMAX >= 4) if (best_kw == 4) return launch_gtc_id_kw<QT, NT, XBF16, 4>(ex, E, N, K, x, ids, M, topk, y, best_s, kseg, best_smem, status, st);
+    if constexpr (KWMAX >= 2) if (best_kw == 2) return launch_gtc_id_kw<QT, NT, XBF16, 2>(ex, E, N, K, x, ids, M, topk, y, best_s, kseg, best_smem, status, st);
+    return launch_gtc_id_kw<QT, NT, XBF16, 1>(ex, E, N, K, x, ids, M, topk, y, best_s, kseg, best_smem, status, st);
+}
+
+struct GtcIdLaunch {
+    bool xbf16;
+    const gtc::IdExperts *ex;
+    int E;
+    int64_t N, K;
+    const void *x;
+    const int32_t *ids;
+    int M, topk;
+    float *y;
+    unsigned int *status;
+    cudaStream_t st;
+    template <int QT> int operator()() {
+        if constexpr (QT <= T_BF16) {
+            return -3;
+        } else {
+            // one 4-token (8 for bf16 activations) column group per pass: an expert rarely gets more
+            if (xbf16) return launch_gtc_id_t<QT, 1, true>(*ex, E, N, K, x, ids, M, topk, y, status, st);
+            return launch_gtc_id_t<QT, 1, false>(*ex, E, N, K, x, ids, M, topk, y, status, st);
+        }
+    }
+};
+
 }  // namespace
 
 // M <= 16 tokens (bigger M is split into groups of 16 by the caller). Returns -3 when the K segments a
@@ -966,6 +1352,16 @@ struct GtcLaunch {
 int launch_gemv_tc(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int M, float *y,
                    unsigned int *status, cudaStream_t st, bool dry) {
     GtcLaunch f{xbf16, wq, N, K, x, M, y, status, st, dry};
+    return dispatch_type(qt, f);
+}
+
+// Expert-indexed product on the tensor-core mat-vec machinery (quantized types). Returns -3 when it does
+// not apply (plain types, or no work split fits on chip); the caller then uses the CUDA-core kernel.
+int launch_gemv_tc_id(int qt, bool xbf16, const void *const *wq, int64_t E, int64_t N, int64_t K, const void *x,
+                      const int32_t *ids, int64_t M, int topk, float *y, unsigned int *status, cudaStream_t st) {
+    gtc::IdExperts ex;
+    for (int e = 0; e < QMM_MAX_EXPERTS; ++e) ex.p[e] = e < E ? static_cast<const uint8_t *>(wq[e]) : nullptr;
+    GtcIdLaunch f{xbf16, &ex, (int)E, N, K, x, ids, (int)M, topk, y, status, st};
     return dispatch_type(qt, f);
 }
 

@@ -14,6 +14,8 @@ int launch_gemv(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const 
                 cudaStream_t st);
 int launch_gemv_tc(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int M, float *y,
                    unsigned int *status, cudaStream_t st, bool dry = false);
+int launch_gemv_tc_id(int qt, bool xbf16, const void *const *wq, int64_t E, int64_t N, int64_t K, const void *x,
+                      const int32_t *ids, int64_t M, int topk, float *y, unsigned int *status, cudaStream_t st);
 int launch_mm(int qt, int tile, const void *wq, int64_t N, int64_t K, const void *x_bf16, int64_t M, float *y,
               float *part, unsigned int *status, cudaStream_t st);
 size_t mm_partial_bytes(int64_t N, int64_t K, int64_t M);
@@ -210,6 +212,9 @@ int qmm_id(const void *const *wq, int64_t E, int qtype, int64_t N, int64_t K, co
     if (!aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(ids) & 3u)) return QMM_EALIGN;
     unsigned int *status = status_ptr();
     if (!status) return QMM_ECUDA;
+    const int rc = launch_gemv_tc_id(qt, (qtype & QMM_X_BF16) != 0, wq, E, N, K, x, ids, M, topk, y, status,
+                                     static_cast<cudaStream_t>(stream));
+    if (rc != -3) return rc;
     return launch_mvid(qt, (qtype & QMM_X_BF16) != 0, wq, E, N, K, x, ids, M, topk, y, status,
                        static_cast<cudaStream_t>(stream));
 }

@@ -329,6 +329,7 @@ def run_ours(args):
                 label, len(idxs), group_ms[gi] * 1e3, wb / (group_ms[gi] * 1e-3) / 1e9,
                 fl / (group_ms[gi] * 1e-3) / 1e12), file=sys.stderr)
     e2e = run_e2e(args, qmm, torch, dev, calls, wq, ws) if not args.case else None
+    moe = run_moe(args, qmm, torch, dev) if (not args.case and not args.no_moe) else None
     cpu = cpu_baseline(args) if (rank == 0 and world == 1 and not args.no_cpu and not args.case) else None
 
     clocks = clk.summary()
@@ -346,11 +347,67 @@ def run_ours(args):
                            COPIES, COPIES * sum(weight_bytes(N, K, qt) for _, N, K, qt in LAYER) / 1e6),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": per_step_launches * args.steps,
-            "clocks": clocks, "per_m": per_m, "peaks": peaks,
+            "clocks": clocks, "per_m": per_m, "moe": moe, "peaks": peaks,
         }
         print(json.dumps(line))
     if pg:
         pg.destroy_process_group()
+
+
+def run_moe(args, qmm, torch, dev):
+    """The expert-indexed product on the MoE workload: 128 experts of 4096 x K Q4_0 (K in {512, 768, 1024}),
+    top-8 routing, n tokens in {1, 2, 4, 8, 12, 16, 24}; 16 id tables (8 distinct experts per token) rotate
+    between calls, and the experts total 151-302 MB per K, beyond the 129 MB L2 at K >= 768. Weights are
+    N(0, 0.02) from torch's seeded CUDA generator (timing only), quantized on the device. Metric: bytes of
+    the distinct experts each call streams / device time (CUDA events over a replayed graph of 32 calls)."""
+    E, N, TOPK, NB, REPS = synthetic.MOE_EXPERTS, synthetic.MOE_ROWS, synthetic.MOE_TOPK, 16, 32
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    stream = torch.cuda.Stream()
+    out, tot_b, tot_t = [], 0.0, 0.0
+    for K in synthetic.MOE_K:
+        rb = qmm.row_bytes("Q4_0", K)
+        wqs = []
+        for _ in range(E):
+            w = torch.randn(N, K, device=dev, generator=gen) * 0.02
+            b = torch.empty(rb * N, dtype=torch.uint8, device=dev)
+            qmm.qmm_quantize(w, "Q4_0", N, K, b)
+            wqs.append(b)
+        for n in synthetic.MOE_TOKENS:
+            tabs = [synthetic.expert_ids(n, batch=b) for b in range(NB)]
+            idss = [torch.from_numpy(t).to(dev) for t in tabs]
+            distinct = [len(np.unique(t)) for t in tabs]
+            x = torch.randn(n, K, device=dev, generator=gen)
+            y = torch.empty(n, TOPK, N, device=dev)
+            with torch.cuda.stream(stream):
+                for i in range(3):
+                    qmm.qmm_id(wqs, "Q4_0", N, K, x, idss[i], y)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(REPS):
+                    qmm.qmm_id(wqs, "Q4_0", N, K, x, idss[i % NB], y)
+            g.replay()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(4):
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (4 * REPS)
+            wbytes = float(np.mean([distinct[i % NB] for i in range(REPS)])) * rb * N
+            out.append({"K": K, "n": n, "us": round(us, 2), "weight_gbs": round(wbytes / us / 1e3, 1)})
+            tot_b += wbytes
+            tot_t += us
+            del g
+        del wqs
+    return {"metric": "expert-indexed weight-GB/s (distinct experts' bytes / time)", "unit": "GB/s",
+            "value": round(tot_b / tot_t / 1e3, 1),
+            "workload": "128 experts x 4096 x K Q4_0, top-8, K in {512,768,1024}, n in {1,2,4,8,12,16,24}",
+            "cases": out}
 
 
 def run_e2e(args, qmm, torch, dev, calls, wq, ws):
@@ -458,6 +515,7 @@ def main():
     ap.add_argument("--case", default=None, help="time one call only, e.g. ffn_gate:2048")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--detail", action="store_true", help="per-call device times on stderr")
+    ap.add_argument("--no-moe", action="store_true", help="skip the expert-indexed (MoE) leg")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

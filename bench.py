@@ -164,6 +164,12 @@ def max_over_ranks(pg, v, device=None):
     return float(t.item())
 
 
+def whole_job(pg, units_per_rank, seconds, world, device=None):
+    """Whole-job throughput of N replicas doing the same work: the units all ranks processed divided by the
+    slowest rank's time."""
+    return units_per_rank * world / max_over_ranks(pg, seconds, device)
+
+
 # ---------------------------------------------------------------------------------------- our arm
 
 def run_ours(args):
@@ -286,8 +292,8 @@ def run_ours(args):
     t_small = sum(call_ms[i] for i in small) * 1e-3
     fl_big = sum(2.0 * calls[i][4] * calls[i][1] * calls[i][2] for i in big)
     t_big = sum(call_ms[i] for i in big) * 1e-3
-    gbs = wb_small / t_small / 1e9 * world if small else None
-    tfl = fl_big / t_big / 1e12 * world if big else None
+    gbs = whole_job(pg, wb_small, t_small, world, dev) / 1e9 if small else None
+    tfl = whole_job(pg, fl_big, t_big, world, dev) / 1e12 if big else None
 
     # dominant call class by time: the tensor-core calls at M >= 512 (or the mat-vec ones)
     dom = [i for i, c in enumerate(calls) if c[4] >= 512]

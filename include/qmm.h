@@ -84,7 +84,8 @@ enum qmm_type {
  * M <= 16 runs the memory-bound mat-vec path (all lanes on weights, narrow-K row split); larger M runs
  * the tcgen05 tensor-core path with a 32/64/128-token tile picked by qmm_pick_tile(M). The tensor-core
  * path rounds x and the dequantized weights to bfloat16 (round to nearest even) and accumulates in
- * binary32; the mat-vec path multiplies the binary32 dequantized weights by x in binary32.
+ * binary32 (for Q4_K, Q5_K and A4G64 the weight rounded is the binary32 weight up to 2^-17 times its
+ * sub-block scale); the mat-vec path multiplies the binary32 dequantized weights by x in binary32.
  * The tensor-core path needs device scratch: M*K*2 bytes for the bfloat16 copy of binary32 x, and, when
  * few 128-row blocks leave most SMs idle and the K dimension is split over CTAs, S*M*N*4 bytes of binary32
  * partial sums (added in a fixed order by a second kernel). qmm() takes the scratch from the stream-ordered

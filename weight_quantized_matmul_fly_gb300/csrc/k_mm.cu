@@ -58,15 +58,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // ------------------------------------------------------------------------------------------ slab decoders
 // A decoder lane turns 32 consecutive weights of one row (chunk c) into 16 bf16x2 words, each the bf16
-// rounding (nearest even) of the binary32 dequantized weight. Raw bytes are loaded one K step ahead.
-// Small codes become binary32 through the 2^23 bias: byte-permute the code under exponent byte 0x4B,
-// subtract 2^23 (exact), then one multiply-add.
-__device__ __forceinline__ float code_f(uint32_t v4, int j) {   // byte j of v4 (< 2^8) as binary32
-    return __int_as_float(__byte_perm(v4, 0x4B000000u, 0x7540u + (uint32_t)j)) - 8388608.0f;
+// rounding (nearest even) of the binary32 dequantized weight. Raw bytes are loaded two K steps ahead.
+// One byte-permute and one multiply-add per weight: the permute puts code byte j (< 128) under exponent
+// byte 0x43, which reads as exactly 128 + q, and the weight ds*q + off is computed as
+// ds*(128 + q) + (off - 128*ds) with the second term formed once per chunk. Where off - 128*ds is exact
+// (the types without an additive term: -(128 + bias)*ds needs at most 21 significant bits) the result is
+// the binary32 weight bit for bit; with an additive term (Q4_K, Q5_K, A4G64) that term is rounded once,
+// an absolute error of at most 2^-17 * ds before the bf16 rounding.
+__device__ __forceinline__ float code128(uint32_t v4, int j) {   // 128 + byte j of v4, exact for bytes < 128
+    return __int_as_float(__byte_perm(v4, 0x43u, 0x4055u | ((uint32_t)j << 8)));
 }
-__device__ __forceinline__ void fma4_pack(uint32_t v4, float s, float o, uint32_t &lo, uint32_t &hi) {
-    lo = pack_bf16x2(__fmaf_rn(s, code_f(v4, 0), o), __fmaf_rn(s, code_f(v4, 1), o));
-    hi = pack_bf16x2(__fmaf_rn(s, code_f(v4, 2), o), __fmaf_rn(s, code_f(v4, 3), o));
+// the four codes of v4 -> bf16x2 (lo: codes 0, 1; hi: codes 2, 3) of s * (128 + q) + c
+__device__ __forceinline__ void fma4_pack(uint32_t v4, float s, float c, uint32_t &lo, uint32_t &hi) {
+    lo = pack_bf16x2(__fmaf_rn(s, code128(v4, 0), c), __fmaf_rn(s, code128(v4, 1), c));
+    hi = pack_bf16x2(__fmaf_rn(s, code128(v4, 2), c), __fmaf_rn(s, code128(v4, 3), c));
 }
 
 template <int QT> struct Slab {
@@ -92,7 +97,7 @@ template <int QT> struct SlabQ45K {
         const int t = c & 7, sh = 4 * (t & 1);
         const float d = h2f(r.hd.x & 0xffffu), dmin = h2f(r.hd.x >> 16);
         const float ds = __fmul_rn(d, u2f_small(six_bits(r.hd.y, r.hd.z, r.hd.w, t)));
-        const float dm = -__fmul_rn(dmin, u2f_small(six_bits(r.hd.y, r.hd.z, r.hd.w, 8 + t)));
+        const float dm = __fmaf_rn(-128.0f, ds, -__fmul_rn(dmin, u2f_small(six_bits(r.hd.y, r.hd.z, r.hd.w, 8 + t))));
         const uint32_t q[8] = {r.q0.x, r.q0.y, r.q0.z, r.q0.w, r.q1.x, r.q1.y, r.q1.z, r.q1.w};
         const uint32_t hh[8] = {r.h0.x, r.h0.y, r.h0.z, r.h0.w, r.h1.x, r.h1.y, r.h1.z, r.h1.w};
 #pragma unroll
@@ -133,19 +138,15 @@ template <> struct Slab<T_Q6_K> {
         const float d = h2f(r.d);
         const float ds0 = __fmul_rn(d, i2f_small((int)(int8_t)(r.sc & 255u)));
         const float ds1 = __fmul_rn(d, i2f_small((int)(int8_t)(r.sc >> 8)));
+        const float c0 = -160.0f * ds0, c1 = -160.0f * ds1;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const uint32_t wl = r.a2 ? __funnelshift_r(r.ql[i], r.ql[i + 1], 16) : r.ql[i];
             const uint32_t wh = r.a2 ? __funnelshift_r(r.qh[i], r.qh[i + 1], 16) : r.qh[i];
             const uint32_t v = ((wl >> shl) & 0x0F0F0F0Fu) | (((wh >> shh) & 0x03030303u) << 4);
-            // (q - 32) * ds: the bias is folded into the subtraction of 2^23 + 32 (exact)
+            // (q - 32) * ds = ds * (128 + q) - 160 * ds, the last term exact
             const float s = i < 4 ? ds0 : ds1;
-            const float f0 = __int_as_float(__byte_perm(v, 0x4B000000u, 0x7540u)) - 8388640.0f;
-            const float f1 = __int_as_float(__byte_perm(v, 0x4B000000u, 0x7541u)) - 8388640.0f;
-            const float f2 = __int_as_float(__byte_perm(v, 0x4B000000u, 0x7542u)) - 8388640.0f;
-            const float f3 = __int_as_float(__byte_perm(v, 0x4B000000u, 0x7543u)) - 8388640.0f;
-            o[2 * i] = pack_bf16x2(__fmul_rn(s, f0), __fmul_rn(s, f1));
-            o[2 * i + 1] = pack_bf16x2(__fmul_rn(s, f2), __fmul_rn(s, f3));
+            fma4_pack(v, s, i < 4 ? c0 : c1, o[2 * i], o[2 * i + 1]);
         }
     }
 };
@@ -163,8 +164,9 @@ template <> struct Slab<T_A4G64> {
     __device__ static void decode(const Raw &r, int c, uint32_t (&o)[16]) {
         const int sh = 4 * (c & 1);
         const float s = bf2f(r.sb & 0xffffu), bias = bf2f(r.sb >> 16);
+        const float cb = __fmaf_rn(-128.0f, s, bias);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) fma4_pack((r.q[i] >> sh) & 0x0F0F0F0Fu, s, bias, o[2 * i], o[2 * i + 1]);
+        for (int i = 0; i < 8; ++i) fma4_pack((r.q[i] >> sh) & 0x0F0F0F0Fu, s, cb, o[2 * i], o[2 * i + 1]);
     }
 };
 
@@ -181,20 +183,11 @@ template <> struct Slab<T_Q4_0> {
     __device__ static void decode(const Raw &r, int c, uint32_t (&o)[16]) {
         (void)c;
         const float d = h2f(r.d);
+        const float cb = -136.0f * d;  // (q - 8) * d = d * (128 + q) - 136 * d, the last term exact
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            // (q - 8) * d, the bias folded into the subtraction of 2^23 + 8
-            const uint32_t lo = r.q[i] & 0x0F0F0F0Fu, hi = (r.q[i] >> 4) & 0x0F0F0F0Fu;
-            float f[4], g[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                f[j] = __fmul_rn(d, __int_as_float(__byte_perm(lo, 0x4B000000u, 0x7540u + j)) - 8388616.0f);
-                g[j] = __fmul_rn(d, __int_as_float(__byte_perm(hi, 0x4B000000u, 0x7540u + j)) - 8388616.0f);
-            }
-            o[2 * i] = pack_bf16x2(f[0], f[1]);
-            o[2 * i + 1] = pack_bf16x2(f[2], f[3]);
-            o[8 + 2 * i] = pack_bf16x2(g[0], g[1]);
-            o[8 + 2 * i + 1] = pack_bf16x2(g[2], g[3]);
+            fma4_pack(r.q[i] & 0x0F0F0F0Fu, d, cb, o[2 * i], o[2 * i + 1]);
+            fma4_pack((r.q[i] >> 4) & 0x0F0F0F0Fu, d, cb, o[8 + 2 * i], o[8 + 2 * i + 1]);
         }
     }
 };

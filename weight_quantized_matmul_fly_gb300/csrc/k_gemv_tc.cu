@@ -1068,6 +1068,9 @@ namespace {
 // Shared memory a CTA may take: two CTAs fit on an SM (228 KB), so one CTA of the next launch in the
 // stream can start streaming its weights while one of this launch still runs.
 constexpr size_t kSmemCap = 110 * 1024;
+// A resident tile may also take up to this much when the split then fits one wave at one CTA per SM (the
+// next launch cannot start its copies early on such an SM, which the work-split cost charges).
+constexpr size_t kSmemBig = 200 * 1024;
 
 // CTAs of this kernel instance that can be resident at once when launched in clusters of S (S = 1: no
 // cluster), for a given dynamic shared memory size; queried once per (S, 4 KB size class) and cached.
@@ -1075,14 +1078,14 @@ template <int QT, int NT, bool XBF16, int KW>
 int64_t gtc_capacity(int64_t S, size_t smem) {
     using LY = gtc::Layout<NT, XBF16>;
     auto kern = gtc::gemv_tc_kernel<QT, NT, XBF16, KW>;
-    constexpr int NCLS = (int)(kSmemCap / 4096) + 1;
+    constexpr int NCLS = (int)(kSmemBig / 4096) + 1;
     static int64_t cache[9][NCLS] = {};
     const int cls = (int)((smem + 4095) / 4096);
     if (S < 1 || S > 8 || cls >= NCLS) return 0;
     if (cache[S][cls]) return cache[S][cls];
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap) != cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBig) != cudaSuccess)
             return 0;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess) return 0;
         attr_set = true;
@@ -1163,7 +1166,7 @@ int launch_gtc_t(const void *wq, int64_t N, int64_t K, const void *x, int M, flo
     // K slices per CTA: more for fewer tokens (the staged activations are then small); only the counts
     // that some M of this column-group count can use are compiled.
     constexpr int KWMAX = NT == 1 ? 8 : ((NT == 2 && !XBF16) ? 2 : 1);
-    int kw_cap = M <= 2 ? 8 : (M <= 8 ? 2 : 1);
+    int kw_cap = M <= 2 ? 8 : (M <= 4 ? 4 : (M <= 8 ? 2 : 1));
     if (kw_cap > KWMAX) kw_cap = KWMAX;
     int best_kw = 1, best_s = 1, best_ns = 1;
     int64_t best_cost = -1, best_ctas = 0;
@@ -1175,36 +1178,45 @@ int launch_gtc_t(const void *wq, int64_t N, int64_t K, const void *x, int M, flo
             const int64_t per_warp = (kseg / 256 + kw - 1) / kw;      // macro blocks per warp (at most)
             const size_t fixed = LY::BARS + LY::xbytes((int)kseg, UNIT, M) + LY::red_bytes((int)S, 8 / kw);
             const size_t tile = LY::tile_bytes(8 / kw, (int)(kseg / 256 * MB_BYTES));
-            int64_t ns = 0;                                           // resident tile if it fits
-            size_t smem = fixed + tile;
-            if (smem > kSmemCap) {
-                if (fixed + LY::ring_bytes(SLOT, 1) > kSmemCap) continue;
-                ns = (int64_t)((kSmemCap - fixed) / LY::ring_bytes(SLOT, 1));
-                if (ns > per_warp) ns = per_warp;
-                if (ns > gtc::NSMAX) ns = gtc::NSMAX;
-                if (ns < 2 && per_warp >= 2) continue;                // no overlap of copies and decoding
-                smem = LY::bytes((int)kseg, UNIT, M, SLOT, (int)ns) + LY::red_bytes((int)S, 8 / kw);
-            }
             const int64_t ctas = nrb * S;
-            int64_t resident = 0;
-            if (kw == 1) resident = gtc_capacity<QT, NT, XBF16, 1>(S, smem);
-            if constexpr (KWMAX >= 2) if (kw == 2) resident = gtc_capacity<QT, NT, XBF16, 2>(S, smem);
-            if constexpr (KWMAX >= 4) if (kw == 4) resident = gtc_capacity<QT, NT, XBF16, 4>(S, smem);
-            if constexpr (KWMAX >= 8) if (kw == 8) resident = gtc_capacity<QT, NT, XBF16, 8>(S, smem);
-            if (resident <= 0) continue;
-            const int64_t waves = (ctas + resident - 1) / resident;
-            // In macro blocks per warp: +2 per wave for its start, the activation staging and the
-            // reduction, +1 more per 4096 activations a CTA stages, +1 for a cluster (its barriers and the
-            // exchange of partial sums cost about as much as a macro block), +1 for a ring (small copies
-            // stream slower than one copy per row).
-            const int64_t cost = waves * (per_warp + 2) + ((int64_t)M * kseg) / 4096 + (S > 1 ? 1 : 0) +
-                                 (ns > 0 ? 1 : 0);
-            if (best_cost < 0 || cost < best_cost || (cost == best_cost && ctas > best_ctas)) {
-                best_cost = cost; best_kw = kw; best_s = (int)S; best_ctas = ctas; best_ns = (int)ns;
+            // candidates: resident tile (two CTAs per SM, or one with a large tile), or a ring
+            auto consider = [&](int64_t ns, size_t smem, int64_t extra) {
+                int64_t resident = 0;
+                if (kw == 1) resident = gtc_capacity<QT, NT, XBF16, 1>(S, smem);
+                if constexpr (KWMAX >= 2) if (kw == 2) resident = gtc_capacity<QT, NT, XBF16, 2>(S, smem);
+                if constexpr (KWMAX >= 4) if (kw == 4) resident = gtc_capacity<QT, NT, XBF16, 4>(S, smem);
+                if constexpr (KWMAX >= 8) if (kw == 8) resident = gtc_capacity<QT, NT, XBF16, 8>(S, smem);
+                if (resident <= 0) return;
+                const int64_t waves = (ctas + resident - 1) / resident;
+                // In macro blocks per warp: +2 per wave for its start, the activation staging and the
+                // reduction, +1 more per 4096 activations a CTA stages, +1 for a cluster (its barriers and
+                // the exchange of partial sums cost about as much as a macro block), plus `extra`.
+                const int64_t cost = waves * (per_warp + 2) + ((int64_t)M * kseg) / 4096 + (S > 1 ? 1 : 0) + extra;
+                if (best_cost < 0 || cost < best_cost || (cost == best_cost && ctas > best_ctas)) {
+                    best_cost = cost; best_kw = kw; best_s = (int)S; best_ctas = ctas; best_ns = (int)ns;
+                }
+            };
+            const size_t smem_res = fixed + tile;
+            if (smem_res <= kSmemCap) {
+                consider(0, smem_res, 0);
+                continue;
             }
+            if (smem_res <= kSmemBig) consider(0, smem_res, 1);    // no overlap with the next launch
+            if (fixed + LY::ring_bytes(SLOT, 1) > kSmemCap) continue;
+            int64_t ns = (int64_t)((kSmemCap - fixed) / LY::ring_bytes(SLOT, 1));
+            if (ns > per_warp) ns = per_warp;
+            if (ns > gtc::NSMAX) ns = gtc::NSMAX;
+            if (ns < 2 && per_warp >= 2) continue;                    // no overlap of copies and decoding
+            // small copies stream slower than one copy per row (measured: about one macro block at one
+            // token, three with more)
+            consider(ns, LY::bytes((int)kseg, UNIT, M, SLOT, (int)ns) + LY::red_bytes((int)S, 8 / kw), M > 1 ? 3 : 1);
         }
     }
     if (best_cost < 0) return -3;                                     // caller splits the tokens
+    // A ring with several column groups streams slower than two launches on halves of the tokens with
+    // resident tiles (measured: ffn_down 2560x9728 Q6_K at 7 tokens 25.6 us as a ring); for matrices
+    // up to 64 MB the caller halves the tokens instead.
+    if (NT > 1 && best_ns > 0 && N * row_bytes(QT, K) < ((int64_t)64 << 20)) return -3;
     if (dry) return 0;                                                // planning only (launch counting)
     const int64_t kseg = ((nmacro + best_s - 1) / best_s) * 256;
     if constexpr (KWMAX >= 8) if (best_kw == 8) return launch_gtc_kw<QT, NT, XBF16, 8>(wq, N, K, x, M, y, best_s, kseg, best_ns, status, st);

@@ -62,3 +62,27 @@ def test_qmm_id_duplicate_and_bad_ids():
     check_tol(y, ref, bnd, TOL_FP32, "dup/bad ids")
     assert np.all(np.isnan(y[1, 1])) and np.all(np.isnan(y[2, 0]))
     assert qmm.qmm_get_status() == 0
+
+
+def test_qmm_id_long_k_cluster_split():
+    """K = 8192 (32 macro blocks): the work split takes 4 K segments per cluster, whose partial sums are
+    added in rank order; 5 tokens routed to 2 of 4 experts."""
+    E, N, K, M, topk = 4, 64, 8192, 5, 2
+    wqs = _experts("Q4_0", E, N, K, seed=77)
+    x = synthetic.activations(M, K, seed=77)
+    ids = synthetic.expert_ids(M, E=E, topk=topk, seed=77)
+    y = _run(wqs, "Q4_0", N, K, x, ids)
+    ref, bnd = oracle.qmm_id("Q4_0", wqs, N, K, x, ids)
+    check_tol(y, ref, bnd, TOL_FP32, "K=8192")
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_qmm_id_many_slots_per_expert(bf16):
+    """64 tokens over 4 experts (about 64 slots each): many passes of 4 (8 for bf16 activations) tokens."""
+    E, N, K, M, topk = 4, 96, 512, 64, 4
+    wqs = _experts("Q4_K", E, N, K, seed=5)
+    x = synthetic.activations(M, K, seed=5, bf16=bf16)
+    ids = synthetic.expert_ids(M, E=E, topk=topk, seed=5)
+    y = _run(wqs, "Q4_K", N, K, x, ids)
+    ref, bnd = oracle.qmm_id("Q4_K", wqs, N, K, x, ids)
+    check_tol(y, ref, bnd, TOL_FP32, "many slots bf16=%s" % bf16)

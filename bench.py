@@ -417,43 +417,64 @@ def run_moe(args, qmm, torch, dev):
 
 
 def run_e2e(args, qmm, torch, dev, calls, wq, ws):
-    """The headline metric end to end through the public API with host buffers: the step's M <= 16 calls,
-    each copying its activations from pinned host memory to the device and its result back to pinned host
-    memory inside the timed region (weights stay resident, as a model's would)."""
-    stream = torch.cuda.current_stream()
+    """The headline metric end to end through the public API with host buffers: every step copies the
+    activations of its M <= 16 calls from pinned host memory to the device (one copy of all of them), runs
+    the calls through qmm_ws, and copies every call's result back to pinned host memory (one copy), all
+    inside the timed region; a step is captured as one CUDA graph per weight copy, as a caller replaying a
+    decode step would (weights stay resident, as a model's do)."""
     small = [c for c in calls if c[4] <= 16]
-    hx, hy, dx, dy = {}, {}, {}, {}
-    for name, N, K, qt, M, b in small:
-        if (M, K) not in hx:
-            hx[(M, K)] = torch.from_numpy(synthetic.activations(M, K, seed=M)).pin_memory()
-            dx[(M, K)] = torch.empty((M, K), dtype=torch.float32, device=dev)
-        if (M, N) not in hy:
-            hy[(M, N)] = torch.empty((M, N), dtype=torch.float32).pin_memory()
-            dy[(M, N)] = torch.empty((M, N), dtype=torch.float32, device=dev)
+    xkeys = sorted({(c[4], c[2]) for c in small})
+    xoff, nx = {}, 0
+    for M, K in xkeys:
+        xoff[(M, K)] = nx
+        nx += M * K
+    yoff, ny = [], 0
+    for c in small:
+        yoff.append(ny)
+        ny += c[4] * c[1]
+    hx = torch.empty(nx, dtype=torch.float32).pin_memory()
+    for M, K in xkeys:
+        hx[xoff[(M, K)]:xoff[(M, K)] + M * K] = torch.from_numpy(synthetic.activations(M, K, seed=M)).reshape(-1)
+    hy = torch.empty(ny, dtype=torch.float32).pin_memory()
+    dx = torch.empty(nx, dtype=torch.float32, device=dev)
+    dy = torch.empty(ny, dtype=torch.float32, device=dev)
 
-    def step(s):
-        for name, N, K, qt, M, b in small:
-            x, y = dx[(M, K)], dy[(M, N)]
-            x.copy_(hx[(M, K)], non_blocking=True)
-            qmm.qmm_ws(wq[(s % COPIES, name)], qt, N, K, x, y, ws)
-            hy[(M, N)].copy_(y, non_blocking=True)
+    def step(copy):
+        dx.copy_(hx, non_blocking=True)
+        for i, (name, N, K, qt, M, b) in enumerate(small):
+            x = dx[xoff[(M, K)]:xoff[(M, K)] + M * K].view(M, K)
+            y = dy[yoff[i]:yoff[i] + M * N].view(M, N)
+            qmm.qmm_ws(wq[(copy, name)], qt, N, K, x, y, ws)
+        hy.copy_(dy, non_blocking=True)
 
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for s in range(3):
+            step(s % COPIES)
+    torch.cuda.synchronize()
+    graphs = []
+    for copy in range(COPIES):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(copy)
+        graphs.append(g)
     steps = max(10, args.steps)
-    for s in range(3):
-        step(s)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for s in range(steps):
-        step(s)
-    e1.record(stream)
-    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for s in range(3):
+            graphs[s % COPIES].replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(steps):
+            graphs[s % COPIES].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     wb = sum(weight_bytes(c[1], c[2], c[3]) for c in small)
     return {"value": round(wb / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
-            "h2d_bytes_per_step": sum(c[4] * c[2] * 4 for c in small),
-            "d2h_bytes_per_step": sum(c[4] * c[1] * 4 for c in small), "steps": steps,
-            "calls": "the 21 calls with M<=16"}
+            "h2d_bytes_per_step": nx * 4, "d2h_bytes_per_step": ny * 4, "steps": steps,
+            "calls": "the 21 calls with M<=16, one host-to-device copy of their activations and one "
+                     "device-to-host copy of their results per step, replayed as CUDA graphs"}
 
 
 # ---------------------------------------------------------------------------------------- oracle legs

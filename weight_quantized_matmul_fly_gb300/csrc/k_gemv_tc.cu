@@ -1079,23 +1079,23 @@ int64_t gtc_capacity(int64_t S, size_t smem) {
     using LY = gtc::Layout<NT, XBF16>;
     auto kern = gtc::gemv_tc_kernel<QT, NT, XBF16, KW>;
     constexpr int NCLS = (int)(kSmemBig / 4096) + 1;
-    static int64_t cache[9][NCLS] = {};
+    static int64_t cache[kMaxDevices][9][NCLS] = {};
+    static bool attr_set[kMaxDevices] = {};
+    const int dev = current_device_index();
     const int cls = (int)((smem + 4095) / 4096);
     if (S < 1 || S > 8 || cls >= NCLS) return 0;
-    if (cache[S][cls]) return cache[S][cls];
-    static bool attr_set = false;
-    if (!attr_set) {
+    if (cache[dev][S][cls]) return cache[dev][S][cls];
+    if (!attr_set[dev]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBig) != cudaSuccess)
             return 0;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess) return 0;
-        attr_set = true;
+        attr_set[dev] = true;
     }
     const size_t smem_q = (size_t)cls * 4096;
     int64_t cap = 0;
     if (S == 1) {
-        int per_sm = 0, dev = 0, sms = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        int per_sm = 0;
+        const int sms = device_sm_count();
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, LY::WARPS * 32, smem_q) == cudaSuccess)
             cap = (int64_t)per_sm * sms;
     } else {
@@ -1114,7 +1114,7 @@ int64_t gtc_capacity(int64_t S, size_t smem) {
         if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) == cudaSuccess) cap = (int64_t)nclusters * S;
     }
     if (cap <= 0) cap = S;          // unknown: assume one cluster at a time rather than fail
-    cache[S][cls] = cap;
+    cache[dev][S][cls] = cap;
     return cap;
 }
 
@@ -1255,11 +1255,12 @@ int launch_gtc_id_kw(const gtc::IdExperts &ex, int E, int64_t N, int64_t K, cons
     using LY = gtc::Layout<NT, XBF16>;
     constexpr int RG = LY::WARPS / KW;
     auto kern = gtc::gemv_tc_id_kernel<QT, NT, XBF16, KW>;
-    static bool attr_set = false;
-    if (!attr_set) {
+    static bool attr_set[kMaxDevices] = {};
+    const int devi = current_device_index();
+    if (!attr_set[devi]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap) != cudaSuccess)
             return -6;
-        attr_set = true;
+        attr_set[devi] = true;
     }
     const int64_t dmax = (int64_t)M * topk < E ? (int64_t)M * topk : E;
     cudaLaunchConfig_t cfg = {};
@@ -1295,13 +1296,7 @@ int launch_gtc_id_t(const gtc::IdExperts &ex, int E, int64_t N, int64_t K, const
     const int64_t ngroups = (N + 15) / 16, nmacro = (K + 255) / 256;
     const int nslot = M * topk;
     const int64_t dmax = nslot < E ? nslot : E;
-    static int nsm = 0;
-    if (!nsm) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0)
-            nsm = 148;
-    }
+    const int nsm = device_sm_count();
     int best_kw = 0, best_s = 1;
     int64_t best_cost = -1;
     size_t best_smem = 0;

@@ -489,13 +489,7 @@ int launch_pdl(const void *kern, dim3 grid, dim3 block, size_t smem, cudaStream_
 // 512 columns (T >= 64) when the CTAs of 512 tokens, times the K split, still fill every SM: each weight
 // slab is then decoded once per 512 tokens instead of 256.
 inline int tiles_per_cta(int T, int64_t N, int64_t M, int S) {
-    static int nsm = 0;
-    if (!nsm) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0)
-            nsm = 148;
-    }
+    const int nsm = device_sm_count();
     const int64_t rowblocks = (N + mm::BM - 1) / mm::BM;
     const bool wide = T >= 64 && rowblocks * ((M + 511) / 512) * S >= nsm;
     int j = (wide ? 512 : 256) / T;
@@ -514,10 +508,11 @@ int launch_mm_t(const void *wq, int64_t N, int64_t K, const void *xb, int64_t M,
     if (!make_x_tmap(&map, xb, M, K, T * J > 256 ? 256 : T * J)) return -6;
     auto kern = mm::mm_kernel<QT, T, J>;
     const int smem = mm::smem_bytes(T * J);
-    static bool attr_set = false;   // once per kernel instance
-    if (!attr_set) {
+    static bool attr_set[kMaxDevices] = {};   // once per kernel instance and device
+    const int devi = current_device_index();
+    if (!attr_set[devi]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -6;
-        attr_set = true;
+        attr_set[devi] = true;
     }
     dim3 grid((unsigned)((N + mm::BM - 1) / mm::BM), (unsigned)((M + T * J - 1) / (T * J)), (unsigned)S);
     const int64_t rb = row_bytes(QT, K);
@@ -577,13 +572,7 @@ struct MmLaunch {
 int mm_ksplit(int64_t N, int64_t K, int64_t M) {
     const int64_t ksteps = (K + mm::BK - 1) / mm::BK;
     const int64_t ctas = ((N + mm::BM - 1) / mm::BM) * ((M + 255) / 256);
-    static int nsm = 0;   // SMs of the current device, queried once
-    if (!nsm) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0)
-            nsm = 148;
-    }
+    const int nsm = device_sm_count();
     const double sms = (double)nsm, t_step_us = 0.5, hbm_bytes_per_us = 6.0e6;
     int best = 1;
     double best_t = -1.0;

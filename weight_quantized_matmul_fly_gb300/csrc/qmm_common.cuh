@@ -29,9 +29,31 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace wqk {
+
+// ------------------------------------------------------------------------------------------ per-device state
+// Kernel attributes and launch-planning caches are kept per device (a process may drive several GPUs).
+constexpr int kMaxDevices = 16;
+// Index of the current device for those caches (0 when it cannot be queried).
+inline int current_device_index() {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) d = 0;
+    return d;
+}
+// SMs of the current device (148 when there is no device to ask, e.g. host-only planning).
+inline int device_sm_count() {
+    static int nsm[kMaxDevices] = {};
+    const int d = current_device_index();
+    if (!nsm[d]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || v <= 0) return 148;
+        nsm[d] = v;
+    }
+    return nsm[d];
+}
 
 enum : int {
     T_F32 = 0, T_F16 = 1, T_BF16 = 2, T_Q4_0 = 3, T_Q4_1 = 4, T_Q5_0 = 5, T_Q5_1 = 6, T_Q8_0 = 7,

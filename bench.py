@@ -477,6 +477,73 @@ def run_e2e(args, qmm, torch, dev, calls, wq, ws):
                      "device-to-host copy of their results per step, replayed as CUDA graphs"}
 
 
+def run_extra(args):
+    """The other workloads, timed per call (not part of the bench line): the all-type sweep on one
+    9728 x 2560 matrix (fp32 activations, M in {1, 16, 64, 512, 2048}) and the Qwen3-0.6B-shaped calls with
+    group-64 affine 4-bit weights (bf16 activations, M in {1, 2, 4, 8, 16}). Each case: weights quantized on
+    the device from torch's seeded CUDA generator (timing only), enough copies to exceed L2, 20 calls per
+    CUDA graph replayed 4 times. Prints one JSON line."""
+    import torch
+    import weight_quantized_matmul_fly_gb300 as qmm
+    qmm.build()
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    stream = torch.cuda.Stream()
+
+    def time_case(qt, N, K, Ms, bf16):
+        wbytes = qmm.row_bytes(qt, K) * N
+        ncopy = max(2, int(300e6 // wbytes) + 1)
+        bufs = []
+        for _ in range(ncopy):
+            w = torch.randn(N, K, device=dev, generator=gen) * 0.02
+            b = torch.empty(wbytes, dtype=torch.uint8, device=dev)
+            qmm.qmm_quantize(w, qt, N, K, b)
+            bufs.append(b)
+            del w
+        out = []
+        for M in Ms:
+            x = torch.randn(M, K, device=dev, generator=gen)
+            if bf16:
+                x = x.to(torch.bfloat16)
+            y = torch.empty((M, N), dtype=torch.float32, device=dev)
+            ws = torch.empty(max(256, qmm.qmm_workspace_size(qt, N, K, M)), dtype=torch.uint8, device=dev)
+            with torch.cuda.stream(stream):
+                for i in range(3):
+                    qmm.qmm_ws(bufs[i % ncopy], qt, N, K, x, y, ws)
+            torch.cuda.synchronize()
+            reps = 20
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(reps):
+                    qmm.qmm_ws(bufs[i % ncopy], qt, N, K, x, y, ws)
+            g.replay()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(4):
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (4 * reps)
+            out.append({"M": M, "us": round(us, 2), "weight_gbs": round(wbytes / us / 1e3, 1),
+                        "tflops": round(2.0 * M * N * K / us / 1e6, 2)})
+            del g
+        del bufs
+        return out
+
+    sweep = {}
+    N, K = synthetic.SWEEP_SHAPE
+    for qt in synthetic.SWEEP_TYPES:
+        sweep[qt] = time_case(qt, N, K, synthetic.SWEEP_TOKENS, False)
+    q06 = {}
+    for name, N, K, qt in synthetic.QWEN3_06B_LAYER:
+        q06[name] = time_case(qt, N, K, synthetic.QWEN3_06B_TOKENS, True)
+    print(json.dumps({"extra": True, "sweep_9728x2560": sweep, "qwen3_06b_a4g64": q06}))
+
+
 # ---------------------------------------------------------------------------------------- oracle legs
 
 def oracle_step_sample():
@@ -551,10 +618,14 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--detail", action="store_true", help="per-call device times on stderr")
     ap.add_argument("--no-moe", action="store_true", help="skip the expert-indexed (MoE) leg")
+    ap.add_argument("--extra", action="store_true",
+                    help="instead of the bench line: time the all-type sweep and the Qwen3-0.6B shapes")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.extra:
+        run_extra(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -46,9 +46,9 @@ WORKLOAD = ("Qwen3-Embedding-4B layer: attn_q 4096x2560 Q4_K, attn_k 1024x2560 Q
 # DRAM traffic per launch of the dominant kernel, from one ncu capture of the bench's own step (see
 # profiles/mm_kernel_qwen3_emb_4b_layer_m512_m2048.md): dram__bytes_read.sum + dram__bytes_write.sum averaged
 # over the 14 mm_kernel launches with M in {512, 2048}. Valid only for the kernel source it was taken on.
-MM_TRAFFIC = {"bytes_per_launch": 21.88e6, "launches": 14,
+MM_TRAFFIC = {"bytes_per_launch": 21.77e6, "launches": 14,
               "source": "weight_quantized_matmul_fly_gb300/csrc/k_mm.cu",
-              "sha256": "e441b8dd443476c77822765ca97356a4d5e6b26b533f52565274a2cb58bf5bc0"}
+              "sha256": "17c5539d4901afcddfd6f414500e3b49cd920b09daca64bc9eb0ff831d0c036b"}
 
 
 def mm_traffic():

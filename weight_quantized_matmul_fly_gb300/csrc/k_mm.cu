@@ -465,6 +465,11 @@ static bool make_x_tmap(CUtensorMap *map, const void *xb, int64_t M, int64_t K, 
     return r == CUDA_SUCCESS;
 }
 
+struct MmPlan {
+    int S;      // K split
+    int cols;   // token columns per CTA
+};
+
 namespace {
 
 // Launch with programmatic stream serialization: the kernel may start while its predecessor in the stream
@@ -485,14 +490,12 @@ int launch_pdl(const void *kern, dim3 grid, dim3 block, size_t smem, cudaStream_
     return cudaLaunchKernelExC(&cfg, kern, argv) == cudaSuccess ? 0 : -6;
 }
 
-// Token tiles per CTA: as many as fit 256 columns, but not more than the tokens need (a power of two).
-// 512 columns (T >= 64) when the CTAs of 512 tokens, times the K split, still fill every SM: each weight
-// slab is then decoded once per 512 tokens instead of 256.
-inline int tiles_per_cta(int T, int64_t N, int64_t M, int S) {
-    const int nsm = device_sm_count();
-    const int64_t rowblocks = (N + mm::BM - 1) / mm::BM;
-    const bool wide = T >= 64 && rowblocks * ((M + 511) / 512) * S >= nsm;
-    int j = (wide ? 512 : 256) / T;
+// Token tiles per CTA for a plan of `cols` token columns per CTA (128, 256 or 512): cols / T tiles, at most
+// 256 columns with 32-token tiles, and not more tiles than the tokens need (a power of two).
+inline int tiles_per_cta(int T, int64_t M, int cols) {
+    int j = cols / T;
+    if (T == 32 && j > 8) j = 8;
+    if (j < 1) j = 1;
     const int64_t need = (M + T - 1) / T;
     while (j > 1 && j / 2 >= need) j /= 2;
     // 3, 5 and 6 tiles too, so that a CTA does not multiply up to twice the tokens it holds
@@ -563,37 +566,49 @@ struct MmLaunch {
 
 }  // namespace
 
-// K split of the tensor-core path, a function of (N, K, M) only (never of the token tile), so that every
-// tile variant adds the same partial sums. CTAs of 128 rows x 256 tokens run in waves of one per SM; a
-// split S multiplies the CTAs and divides each CTA's K steps, and costs S*M*N*4 bytes of partial sums
-// written and read back. The split minimises
-//     ceil(ctas * S / SMs) * ceil(ksteps / S) * t_step  +  (2 S M N * 4 bytes) / HBM bandwidth
-// with t_step about 0.5 us (one K step of a full CTA) and splits of at least 4 K steps.
-int mm_ksplit(int64_t N, int64_t K, int64_t M) {
+// Work plan of the tensor-core path: the K split S and the token columns per CTA (128, 256 or 512), a
+// function of (type, N, K, M) only, never of the token tile, so that every tile variant adds the same
+// partial sums in the same order. CTAs of 128 rows run one per SM; the plan minimises the modelled time
+//     waves * (t_wave + ksteps_per_split * t_step(cols, type))  +  (2 S M N * 4 bytes) / HBM bandwidth,
+// where a wave is ceil(CTAs / SMs) and the last term is the partial sums written and read back when K is
+// split. The constants were fitted (about 7 % rms) to a sweep of every split S <= 12 and 128/256/512
+// columns over the seven Qwen3-Embedding-4B projections at 128, 512 and 2048 tokens on GB300: a K step
+// (64 weights) of a CTA costs 0.45 / 0.49 / 0.71 us at 128 / 256 / 512 columns for 4-bit K-quants (the
+// weight decoding, not the tensor core, sets the pace below 512 columns), 1.7 times that for Q6_K, and a
+// wave about 1.4 us to start and drain. Splits keep at least 4 K steps each and leave no split empty.
+MmPlan mm_plan(int qt, int64_t N, int64_t K, int64_t M) {
     const int64_t ksteps = (K + mm::BK - 1) / mm::BK;
-    const int64_t ctas = ((N + mm::BM - 1) / mm::BM) * ((M + 255) / 256);
-    const int nsm = device_sm_count();
-    const double sms = (double)nsm, t_step_us = 0.5, hbm_bytes_per_us = 6.0e6;
-    int best = 1;
+    const int64_t rowblocks = (N + mm::BM - 1) / mm::BM;
+    const int64_t nsm = device_sm_count();
+    const double t_wave = 1.4, hbm_bytes_per_us = 6.0e6;
+    const double type_factor = qt == T_Q6_K ? 1.7 : 1.0;
+    MmPlan best{1, 128};
     double best_t = -1.0;
-    for (int S = 1; S <= 32; ++S) {
-        if (S > 1 && ksteps / S < 4) break;
-        const int64_t waves = (int64_t)((ctas * S + (int64_t)sms - 1) / (int64_t)sms);
-        const int64_t steps = (ksteps + S - 1) / S;
-        double t = (double)waves * (double)steps * t_step_us;
-        if (S > 1) t += 2.0 * S * (double)M * (double)N * 4.0 / hbm_bytes_per_us;
-        if (best_t < 0 || t < best_t * 0.98) { best_t = t; best = S; }
+    for (int cols : {128, 256, 512}) {
+        if (cols > 128 && cols / 2 >= M) break;      // more columns than the tokens need
+        const double t_step = type_factor * (cols == 128 ? 0.45 : (cols == 256 ? 0.49 : 0.71));
+        const int64_t ctas1 = rowblocks * ((M + cols - 1) / cols);
+        for (int S = 1; S <= 32; ++S) {
+            const int64_t kps = (ksteps + S - 1) / S;
+            if (S > 1 && (ksteps / S < 4 || (S - 1) * kps >= ksteps)) continue;
+            const int64_t waves = (ctas1 * S + nsm - 1) / nsm;
+            double t = (double)waves * (t_wave + (double)kps * t_step);
+            if (S > 1) t += 2.0 * S * (double)M * (double)N * 4.0 / hbm_bytes_per_us;
+            if (best_t < 0 || t < best_t * 0.98) { best_t = t; best = MmPlan{S, cols}; }
+        }
     }
     return best;
 }
+
+int mm_ksplit(int qt, int64_t N, int64_t K, int64_t M) { return mm_plan(qt, N, K, M).S; }
 
 // Partial buffers of the K splits are M*N binary32 each, padded to a multiple of 4 elements so that every
 // split starts 16-byte aligned.
 static inline int64_t split_stride_of(int64_t M, int64_t N) { return (M * N + 3) & ~(int64_t)3; }
 
 // Bytes of split-K partials needed (0 when the K dimension is not split).
-size_t mm_partial_bytes(int64_t N, int64_t K, int64_t M) {
-    const int S = mm_ksplit(N, K, M);
+size_t mm_partial_bytes(int qt, int64_t N, int64_t K, int64_t M) {
+    const int S = mm_ksplit(qt, N, K, M);
     return S > 1 ? (size_t)S * (size_t)split_stride_of(M, N) * 4 : 0;
 }
 
@@ -601,12 +616,13 @@ size_t mm_partial_bytes(int64_t N, int64_t K, int64_t M) {
 // dimension is split) holds S * M * N binary32.
 int launch_mm(int qt, int tile, const void *wq, int64_t N, int64_t K, const void *x_bf16, int64_t M, float *y,
               float *part, unsigned int *status, cudaStream_t st) {
-    const int S = mm_ksplit(N, K, M);
+    const MmPlan plan = mm_plan(qt, N, K, M);
+    const int S = plan.S;
     const int64_t ksteps = (K + mm::BK - 1) / mm::BK;
     const int kps = (int)((ksteps + S - 1) / S);
     float *out = S > 1 ? part : y;
     const int64_t sstride = split_stride_of(M, N);
-    MmLaunch f{tile, tiles_per_cta(tile, N, M, S), wq, N, K, x_bf16, M, out, S, kps, sstride, status, st};
+    MmLaunch f{tile, tiles_per_cta(tile, M, plan.cols), wq, N, K, x_bf16, M, out, S, kps, sstride, status, st};
     int rc = dispatch_type(qt, f);
     if (rc || S == 1) return rc;
     const int64_t n = M * N, n4 = n / 4;

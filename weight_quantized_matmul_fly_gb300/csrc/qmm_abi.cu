@@ -18,8 +18,8 @@ int launch_gemv_tc_id(int qt, bool xbf16, const void *const *wq, int64_t E, int6
                       const int32_t *ids, int64_t M, int topk, float *y, unsigned int *status, cudaStream_t st);
 int launch_mm(int qt, int tile, const void *wq, int64_t N, int64_t K, const void *x_bf16, int64_t M, float *y,
               float *part, unsigned int *status, cudaStream_t st);
-size_t mm_partial_bytes(int64_t N, int64_t K, int64_t M);
-int mm_ksplit(int64_t N, int64_t K, int64_t M);
+size_t mm_partial_bytes(int qt, int64_t N, int64_t K, int64_t M);
+int mm_ksplit(int qt, int64_t N, int64_t K, int64_t M);
 int launch_x_to_bf16(const float *x, void *out, int64_t n, cudaStream_t st);
 int launch_mvid(int qt, bool xbf16, const void *const *wq, int64_t E, int64_t N, int64_t K, const void *x,
                 const int32_t *ids, int64_t M, int topk, float *y, unsigned int *status, cudaStream_t st);
@@ -104,7 +104,7 @@ size_t ws_x_bytes(int qtype, int64_t K, int64_t M) {
 }
 size_t ws_bytes(int qtype, int64_t N, int64_t K, int64_t M, int path) {
     if (path == 0) return 0;
-    return ws_x_bytes(qtype, K, M) + align256(mm_partial_bytes(N, K, M));
+    return ws_x_bytes(qtype, K, M) + align256(mm_partial_bytes(qtype & 0xff, N, K, M));
 }
 
 int run_mm(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, float *y, int tile,
@@ -269,7 +269,7 @@ int qmm_launch_count(int qtype, int64_t N, int64_t K, int64_t M) {
                                   nullptr, &n);
         return rc ? (int)((M + 15) / 16) : n;
     }
-    const int S = mm_ksplit(N, K, M);
+    const int S = mm_ksplit(qtype & 0xff, N, K, M);
     return ((qtype & QMM_X_BF16) ? 0 : 1) + 1 + (S > 1 ? 1 + ((M * N) % 4 ? 1 : 0) : 0);
 }
 

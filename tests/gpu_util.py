@@ -42,3 +42,11 @@ def check_tol(y_gpu, y_ref, bound, tol, what=""):
         raise AssertionError("%s: %d of %d outside tolerance; worst err %.3g vs bound %.3g (ratio %.3g)" % (
             what, int(bad.sum()), int(ok.sum()), err[i], bound[ok][i], err[i] / max(bound[ok][i], 1e-300)))
     return float(np.max(err / np.maximum(bound[ok], 1e-300))) if err.size else 0.0
+
+
+def bit_differences(a, b) -> int:
+    """Number of binary32 outputs whose bit patterns differ (the tile-invariance criterion)."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    b = np.ascontiguousarray(b, dtype=np.float32)
+    assert a.shape == b.shape
+    return int(np.sum(a.view(np.uint32) != b.view(np.uint32)))

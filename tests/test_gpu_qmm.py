@@ -9,7 +9,7 @@ import pytest
 import oracle
 import synthetic
 import weight_quantized_matmul_fly_gb300 as qmm
-from gpu_util import TOL_BF16, TOL_FP32, check_tol, dev, torch_cuda, x_dev
+from gpu_util import TOL_BF16, TOL_FP32, bit_differences, check_tol, dev, torch_cuda, x_dev
 
 pytestmark = pytest.mark.gpu
 TYPES = oracle.TYPES
@@ -127,6 +127,6 @@ def test_tile_invariance(qtype):
             outs = [_run(qmm.qmm_with_tile, wq, qtype, N, K, x, tile=t) for t in (32, 64, 128)]
             assert np.any(outs[0] != 0), "all-zero output"
             for t, o in zip((64, 128), outs[1:]):
-                d = int(np.sum(o.view(np.uint32) != outs[0].view(np.uint32)))
+                d = bit_differences(o, outs[0])
                 assert d == 0, "%s %dx%dx%dx%d: %d of %d outputs differ between tiles 32 and %d" % (
                     qtype, batch, M, N, K, d, o.size, t)

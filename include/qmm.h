@@ -87,8 +87,8 @@ enum qmm_type {
  * binary32 (for Q4_K, Q5_K and A4G64 the weight rounded is the binary32 weight up to 2^-17 times its
  * sub-block scale); the mat-vec path multiplies the binary32 dequantized weights by x in binary32.
  * The tensor-core path needs device scratch: M*K*2 bytes for the bfloat16 copy of binary32 x, and, when
- * few 128-row blocks leave most SMs idle and the K dimension is split over CTAs, S*M*N*4 bytes of binary32
- * partial sums (added in a fixed order by a second kernel). qmm() takes the scratch from the stream-ordered
+ * its work plan (a function of the type, N, K and M) splits the K dimension over S CTAs, S*M*N*4 bytes of
+ * binary32 partial sums (added in a fixed order by a second kernel). qmm() takes the scratch from the stream-ordered
  * allocator (cudaMallocAsync / cudaFreeAsync on `stream`); callers that manage memory themselves use
  * qmm_ws() with qmm_workspace_size() bytes.
  */

@@ -43,9 +43,9 @@ WORKLOAD = ("Qwen3-Embedding-4B layer: attn_q 4096x2560 Q4_K, attn_k 1024x2560 Q
             "weights N(0,0.02) quantized")
 
 
-# DRAM traffic per launch of the dominant kernel, from one ncu capture of the bench's own step (see
-# profiles/mm_kernel_qwen3_emb_4b_layer_m512_m2048.md): dram__bytes_read.sum + dram__bytes_write.sum averaged
-# over the 14 mm_kernel launches with M in {512, 2048}. Valid only for the kernel source it was taken on.
+# DRAM traffic per launch of the dominant kernel, from one ncu capture of the bench's own step
+# (`--steps 1 --warmup 3 --no-cpu --no-moe`): dram__bytes_read.sum + dram__bytes_write.sum averaged over the
+# 14 mm_kernel launches with M in {512, 2048}. Valid only for the kernel source it was taken on.
 MM_TRAFFIC = {"bytes_per_launch": 21.77e6, "launches": 14,
               "source": "weight_quantized_matmul_fly_gb300/csrc/k_mm.cu",
               "sha256": "17c5539d4901afcddfd6f414500e3b49cd920b09daca64bc9eb0ff831d0c036b"}

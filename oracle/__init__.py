@@ -63,10 +63,12 @@ def _load():
         lib.orc_dequant_f64.argtypes = [I, P, I64, I64, P]
         lib.orc_dequant_f32.argtypes = [I, P, I64, I64, P]
         lib.orc_qmm.argtypes = [I, I, P, I64, I64, P, I64, P, P]
+        lib.orc_matmul_f64.argtypes = [P, I64, I64, I, P, I64, P, P]
         lib.orc_qmm_sampled.argtypes = [I, I, P, I64, I64, P, I64, I64, P, P, P, P]
         lib.orc_qmm_id.argtypes = [I, I, P, I64, I64, I64, P, P, I64, I, P, P]
+        lib.orc_qmm_id_slots.argtypes = [I, I, P, I64, I64, I64, P, P, I64, I, P, P]
         for f in ("orc_type_info", "orc_quantize", "orc_dequant_f64", "orc_dequant_f32", "orc_qmm",
-                  "orc_qmm_sampled", "orc_qmm_id"):
+                  "orc_qmm_sampled", "orc_qmm_id", "orc_qmm_id_slots", "orc_matmul_f64"):
             getattr(lib, f).restype = I
         _lib = lib
     return _lib
@@ -162,6 +164,21 @@ def qmm(qtype, wq: np.ndarray, N: int, K: int, x: np.ndarray):
     return y, bnd
 
 
+def matmul_f64(w: np.ndarray, x: np.ndarray):
+    """The product step alone on an (N, K) binary64 matrix of decoded weights (e.g. dequant_f64's):
+    (y, bound) as qmm() returns them."""
+    x, xb = _x_arg(x)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    N, K = w.shape
+    M = x.shape[0]
+    assert x.shape == (M, K)
+    y = np.empty((M, N), dtype=np.float64)
+    bnd = np.empty((M, N), dtype=np.float64)
+    if _load().orc_matmul_f64(_ptr(w), N, K, xb, _ptr(x), M, _ptr(y), _ptr(bnd)) != 0:
+        raise ValueError("matmul_f64: out of memory")
+    return y, bnd
+
+
 def qmm_sampled(qtype, wq: np.ndarray, N: int, K: int, x: np.ndarray, ms, ns):
     """The same sums for the listed (m, n) pairs only."""
     x, xb = _x_arg(x)
@@ -178,18 +195,22 @@ def qmm_sampled(qtype, wq: np.ndarray, N: int, K: int, x: np.ndarray, ms, ns):
 
 
 def qmm_id(qtype, wqs, N: int, K: int, x: np.ndarray, ids: np.ndarray):
-    """Expert-indexed product. wqs: list of E (N, row_bytes) uint8 arrays. Returns (y, bound) of shape
+    """Expert-indexed product. wqs: list of E (N, row_bytes) uint8 arrays; x is (M, K), one row per token
+    shared by its slots, or (M, topk, K), one row per (token, slot). Returns (y, bound) of shape
     (M, topk, N)."""
+    per_slot = x.ndim == 3
     x, xb = _x_arg(x)
     M = x.shape[0]
     ids = np.ascontiguousarray(ids, dtype=np.int32)
     topk = ids.shape[1]
+    assert x.shape == ((M, topk, K) if per_slot else (M, K))
     wqs = [np.ascontiguousarray(w, dtype=np.uint8) for w in wqs]
     ptrs = (ctypes.c_void_p * len(wqs))(*[w.ctypes.data for w in wqs])
     y = np.empty((M, topk, N), dtype=np.float64)
     bnd = np.empty((M, topk, N), dtype=np.float64)
-    rc = _load().orc_qmm_id(_qt(qtype), xb, ctypes.cast(ptrs, ctypes.c_void_p), len(wqs), N, K, _ptr(x),
-                            _ptr(ids), M, topk, _ptr(y), _ptr(bnd))
+    fn = _load().orc_qmm_id_slots if per_slot else _load().orc_qmm_id
+    rc = fn(_qt(qtype), xb, ctypes.cast(ptrs, ctypes.c_void_p), len(wqs), N, K, _ptr(x), _ptr(ids), M, topk,
+            _ptr(y), _ptr(bnd))
     if rc != 0:
         raise ValueError("qmm_id: bad arguments")
     return y, bnd

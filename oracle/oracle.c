@@ -16,7 +16,9 @@
  *     method reaches is the plain definition above, which is what this file writes out.
  *   - The expert-indexed product y[t, j, :] = W_{ids[t, j]} x[t, :] (llama.cpp PR 28086, "metal : fix
  *     idle threads in mul_mv_iq3_xxs for ne00 < 1024", sections "Overview" and "Additional
- *     information": MUL_MAT_ID, one mat-vec per routed expert).
+ *     information": MUL_MAT_ID, one mat-vec per routed expert), and its form with one activation row per
+ *     (token, slot), y[t, j, :] = W_{ids[t, j]} x[t, j, :] (the same page, "Test methodology": the
+ *     experts' down projection, ffn_down_exps, whose input differs per routed expert).
  *   - The block layouts, the exact decoding rule and the deterministic encoder: the pages name the types
  *     (candle PR 4056, section "What changes"; tiny-llm PR 122, "Summary") but define none of them, so
  *     they follow this repository's block-format specification, sections 2 to 4.
@@ -509,17 +511,14 @@ static double x_at(const void *x, int xbf16, int64_t idx)
 }
 
 /*
- * y64[m*N + n] = sum_k w[n,k] x[m,k], k ascending, binary64; bound[m*N + n] = sum_k |w[n,k] x[m,k]|.
- * w is the exact decoded matrix. Either output pointer may be NULL.
+ * The product on decoded weights: y64[m*N + n] = sum_k w[n,k] x[m,k], k ascending, binary64;
+ * bound[m*N + n] = sum_k |w[n,k] x[m,k]|. w is an N x K binary64 matrix. Either output may be NULL.
  */
-int orc_qmm(int qt, int xbf16, const uint8_t *wq, int64_t N, int64_t K, const void *x, int64_t M,
-            double *y64, double *bound)
+int orc_matmul_f64(const double *w, int64_t N, int64_t K, int xbf16, const void *x, int64_t M, double *y64,
+                   double *bound)
 {
-    if (qt < 0 || qt >= T_COUNT || K % QK[qt] != 0) return -1;
-    double *w = (double *)malloc((size_t)(N * K) * sizeof(double));
     double *xd = (double *)malloc((size_t)(M * K) * sizeof(double));
-    if (!w || !xd) { free(w); free(xd); return -2; }
-    orc_dequant_f64(qt, wq, N, K, w);
+    if (!xd) return -2;
     for (int64_t i = 0; i < M * K; i++) xd[i] = x_at(x, xbf16, i);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t n = 0; n < N; n++) {
@@ -534,9 +533,21 @@ int orc_qmm(int qt, int xbf16, const uint8_t *wq, int64_t N, int64_t K, const vo
             if (bound) bound[m * N + n] = a;
         }
     }
-    free(w);
     free(xd);
     return 0;
+}
+
+/* The whole method: decode every block exactly (orc_dequant_f64), then the product above. */
+int orc_qmm(int qt, int xbf16, const uint8_t *wq, int64_t N, int64_t K, const void *x, int64_t M,
+            double *y64, double *bound)
+{
+    if (qt < 0 || qt >= T_COUNT || K % QK[qt] != 0) return -1;
+    double *w = (double *)malloc((size_t)(N * K) * sizeof(double));
+    if (!w) return -2;
+    orc_dequant_f64(qt, wq, N, K, w);
+    int rc = orc_matmul_f64(w, N, K, xbf16, x, M, y64, bound);
+    free(w);
+    return rc;
 }
 
 /* The same sums for a list of (m, n) pairs only: decode just the rows asked for. */
@@ -567,11 +578,15 @@ int orc_qmm_sampled(int qt, int xbf16, const uint8_t *wq, int64_t N, int64_t K, 
 }
 
 /*
- * Expert-indexed product: y64[(t*topk + j)*N + n] = sum_k W_e[n,k] x[t,k] with e = ids[t*topk + j].
+ * Expert-indexed product: y64[(t*topk + j)*N + n] = sum_k W_e[n,k] x[r,k] with e = ids[t*topk + j], where
+ * the activation row r is the token's, r = t (one row per token, shared by its topk slots), or the slot's
+ * own, r = t*topk + j (x_per_slot: each routed pair has its own input row, as the down projection of the
+ * experts has; llama.cpp PR 28086, "Test methodology", ffn_down_exps).
  * wq[e] points at expert e's N x K block matrix. An id outside [0, E) gives NaN for that slot.
  */
-int orc_qmm_id(int qt, int xbf16, const uint8_t *const *wq, int64_t E, int64_t N, int64_t K, const void *x,
-               const int32_t *ids, int64_t M, int topk, double *y64, double *bound)
+static int qmm_id_rows(int qt, int xbf16, const uint8_t *const *wq, int64_t E, int64_t N, int64_t K,
+                       const void *x, int x_per_slot, const int32_t *ids, int64_t M, int topk, double *y64,
+                       double *bound)
 {
     if (qt < 0 || qt >= T_COUNT || K % QK[qt] != 0) return -1;
     int64_t nb = K / QK[qt];
@@ -591,7 +606,7 @@ int orc_qmm_id(int qt, int xbf16, const uint8_t *const *wq, int64_t E, int64_t N
                 orc_dequant_f64(qt, wq[e] + n * rowbytes, 1, K, w);
                 double s = 0.0, a = 0.0;
                 for (int64_t k = 0; k < K; k++) {
-                    double pr = w[k] * x_at(x, xbf16, t * K + k);
+                    double pr = w[k] * x_at(x, xbf16, (x_per_slot ? t * topk + j : t) * K + k);
                     s += pr;
                     a += fabs(pr);
                 }
@@ -602,4 +617,17 @@ int orc_qmm_id(int qt, int xbf16, const uint8_t *const *wq, int64_t E, int64_t N
         }
     }
     return 0;
+}
+
+int orc_qmm_id(int qt, int xbf16, const uint8_t *const *wq, int64_t E, int64_t N, int64_t K, const void *x,
+               const int32_t *ids, int64_t M, int topk, double *y64, double *bound)
+{
+    return qmm_id_rows(qt, xbf16, wq, E, N, K, x, 0, ids, M, topk, y64, bound);
+}
+
+/* The same with one activation row per (token, slot): x is M x topk x K. */
+int orc_qmm_id_slots(int qt, int xbf16, const uint8_t *const *wq, int64_t E, int64_t N, int64_t K,
+                     const void *x, const int32_t *ids, int64_t M, int topk, double *y64, double *bound)
+{
+    return qmm_id_rows(qt, xbf16, wq, E, N, K, x, 1, ids, M, topk, y64, bound);
 }

@@ -162,3 +162,48 @@ def test_expert_ids_distinct(orc):
     assert ids.shape == (24, 8)
     assert all(len(set(r)) == 8 for r in ids.tolist())
     assert ids.min() >= 0 and ids.max() < 128
+
+
+def test_qmm_id_slots_unit_scale_is_integer_matmul(orc):
+    """Per-slot activations (x of shape M x topk x K): with Q8_0 blocks of scale 1 and integer
+    activations, slot (t, j) is the exact integer product of expert ids[t, j]'s codes with its own row
+    x[t, j]; a slip to the token's first row, or to the wrong expert, changes the integers."""
+    g = np.random.default_rng(12)
+    E, N, K, M, topk = 4, 7, 64, 3, 2
+    codes = [g.integers(-128, 128, (N, K)) for _ in range(E)]
+    wqs = []
+    for e in range(E):
+        blocks = [sf.pack("Q8_0", {"d": sf.h16(1.0), "q": [int(c) for c in codes[e][n, 32 * b:32 * b + 32]]})
+                  for n in range(N) for b in range(K // 32)]
+        wqs.append(np.frombuffer(b"".join(blocks), dtype=np.uint8).copy())
+    xi = g.integers(-50, 51, (M, topk, K))
+    ids = np.array([[0, 3], [2, 2], [1, 0]], dtype=np.int32)
+    y, bnd = orc.qmm_id("Q8_0", wqs, N, K, xi.astype(np.float32), ids)
+    for t in range(M):
+        for j in range(topk):
+            c = codes[ids[t, j]]
+            assert np.array_equal(y[t, j], (c @ xi[t, j]).astype(np.float64))
+            assert np.array_equal(bnd[t, j], (np.abs(c) @ np.abs(xi[t, j])).astype(np.float64))
+
+
+def test_qmm_id_slots_bad_id_gives_nan(orc):
+    E, N, K = 2, 4, 32
+    wqs = [orc.quantize("Q4_0", synthetic.weights(N, K, seed=e)) for e in range(E)]
+    x = synthetic.activations(3, K, seed=1).reshape(1, 3, K)
+    y, _ = orc.qmm_id("Q4_0", wqs, N, K, x, np.array([[1, 2, -1]], dtype=np.int32))
+    assert np.all(np.isfinite(y[0, 0])) and np.all(np.isnan(y[0, 1])) and np.all(np.isnan(y[0, 2]))
+
+
+def test_matmul_step_alone(orc):
+    """The product step on decoded weights: the plain definition checked against numpy's binary64 x @ W.T
+    (within its rounding bound), and the two-step form equals the one-call form bit for bit."""
+    N, K, M = 30, 512, 4
+    w = synthetic.weights(N, K, seed=13)
+    x = synthetic.activations(M, K, seed=13)
+    wq = orc.quantize("Q4_K", w)
+    W = orc.dequant_f64("Q4_K", wq, N, K)
+    y, bnd = orc.matmul_f64(W, x)
+    refb = np.abs(x.astype(np.float64)) @ np.abs(W).T
+    assert np.all(np.abs(y - x.astype(np.float64) @ W.T) <= 2 * K * EPS64 * refb)
+    y1, b1 = orc.qmm("Q4_K", wq, N, K, x)
+    assert np.array_equal(y, y1) and np.array_equal(bnd, b1)

@@ -60,6 +60,10 @@ enum qmm_type {
 
 /* OR into `qtype` to pass bfloat16 activations instead of binary32. */
 #define QMM_X_BF16 0x100
+/* qmm_id only: OR into `qtype` when x holds one activation row per (token, slot), M x topk x K, instead
+ * of one row per token shared by its topk slots (the experts' down projection, whose input differs per
+ * routed expert: llama.cpp PR 28086, "Test methodology", ffn_down_exps). */
+#define QMM_X_PER_SLOT 0x200
 
 /* Error codes. */
 #define QMM_OK 0
@@ -132,9 +136,11 @@ int qmm_noalloc(const void *wq, int qtype, int64_t N, int64_t K, const void *x, 
 
 /*
  * qmm_id: expert-indexed mat-vec (MoE).  For each token t < M and slot j < topk, with e = ids[t*topk + j]:
- *     y[(t*topk + j)*N + n] = sum_k dequant(W_e)[n, k] * x[t*K + k]
+ *     y[(t*topk + j)*N + n] = sum_k dequant(W_e)[n, k] * x[r*K + k]
+ * where the activation row is r = t, or r = t*topk + j when qtype has QMM_X_PER_SLOT.
  *   wq    HOST array of E device pointers, one N x K weight matrix of type qtype per expert
  *         (each 16-byte aligned). The array itself is read during the call only.
+ *   x     M x K (or M x topk x K with QMM_X_PER_SLOT) row-major, binary32 or bfloat16 (QMM_X_BF16).
  *   ids   DEVICE int32 array, M x topk.
  *   y     M x topk x N binary32, overwritten.
  * Every distinct expert's rows are streamed once per call for all tokens routed to it. An id outside
@@ -185,10 +191,27 @@ int qmm_quantize(const float *w_in, int qtype, int64_t N, int64_t K, void *wq_ou
 /* Block size in weights and bytes per block of a type (host only). */
 int qmm_type_info(int qtype, int *block_weights, int *block_bytes);
 
-/* Device status word, a bit set of QMM_STATUS_*: read (synchronising `stream`) and clear. */
+/*
+ * qmm_get_status: the device status word, a bit set of QMM_STATUS_* accumulated by the kernels since the
+ * last call, read and cleared on `stream` (the call synchronises the stream). Returns the bits (>= 0), or
+ * QMM_ECUDA when the read failed. The word is per device and shared by every stream and caller.
+ */
 #define QMM_STATUS_BAD_ID 0x1    /* qmm_id met an expert id outside [0, E) */
-#define QMM_STATUS_TIMEOUT 0x2   /* a bounded wait in a tensor-core kernel gave up */
-int qmm_get_status(void *stream, unsigned int *status);
+#define QMM_STATUS_TIMEOUT 0x2   /* a bounded wait in a kernel gave up (about one second); that call's
+                                    output is incomplete, the device stays usable */
+int qmm_get_status(void *stream);
+
+/*
+ * qmm_debug_stall (test/diagnostic only): qmm() on the mat-vec path (a quantized type, M <= 16) with
+ * the warps of the first thread block made to wait for their first weight stage on a barrier that nothing
+ * signals. Those bounded waits run out after about one second: each such warp records QMM_STATUS_TIMEOUT,
+ * waits (bounded) for the weight copies still in flight into its shared memory, skips its share of the
+ * work, and the kernel returns normally, so y is incomplete but the device and later calls are
+ * unaffected. Exists to test the failure path without faulting or hanging a GPU. Returns QMM_ERANGE for
+ * plain types or M > 16.
+ */
+int qmm_debug_stall(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, float *y,
+                    void *stream);
 
 const char *qmm_strerror(int code);
 

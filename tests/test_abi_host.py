@@ -80,6 +80,20 @@ def test_qmm_id_errors(L):
     assert L.qmm_id(ctypes.cast(bad, P), 2, 3, 64, 64, P(A), P(A), 1, 8, P(A), None) == -5
 
 
+def test_qmm_id_flags(L):
+    ptrs = (ctypes.c_void_p * 2)(A, A)
+    arr = ctypes.cast(ptrs, P)
+    assert L.qmm_id(arr, 2, 3 | 0x400, 64, 64, P(A), P(A), 1, 8, P(A), None) == -1   # unknown flag
+    assert L.qmm_id(arr, 2, 3 | 0x200, 64, 48, P(A), P(A), 1, 8, P(A), None) == -2   # per-slot x accepted
+    assert L.qmm(P(A), 3 | 0x200, 64, 64, P(A), 1, P(A), None) == -1                # not a qmm flag
+
+
+def test_debug_stall_errors(L):
+    assert L.qmm_debug_stall(P(A), 0, 64, 64, P(A), 1, P(A), None) == -7    # plain type: no such path
+    assert L.qmm_debug_stall(P(A), 3, 64, 64, P(A), 17, P(A), None) == -7   # tensor-core path
+    assert L.qmm_debug_stall(P(A), 3, 64, 64, None, 1, P(A), None) == -4
+
+
 def test_dequant_quantize_errors(L):
     assert L.qmm_dequant(P(A), 20, 4, 64, P(A), None) == -1
     assert L.qmm_dequant(P(A), 3, 4, 40, P(A), None) == -2

@@ -86,3 +86,23 @@ def test_qmm_id_many_slots_per_expert(bf16):
     y = _run(wqs, "Q4_K", N, K, x, ids)
     ref, bnd = oracle.qmm_id("Q4_K", wqs, N, K, x, ids)
     check_tol(y, ref, bnd, TOL_FP32, "many slots bf16=%s" % bf16)
+
+
+@pytest.mark.parametrize("qtype", ["Q4_0", "Q4_K", "Q6_K", "A4G64", "F16", "BF16"])
+@pytest.mark.parametrize("M", [1, 5, 24])
+def test_qmm_id_per_slot_activations(qtype, M):
+    """x of shape M x topk x K (one activation row per routed pair, the experts' down projection:
+    llama.cpp PR 28086, "Test methodology", ffn_down_exps), on both expert kernels."""
+    E, N, K, topk = 12, 140, 512, 8
+    wqs = _experts(qtype, E, N, K, seed=60)
+    bf16 = qtype == "A4G64"
+    x = synthetic.activations(M * topk, K, seed=M + 60, bf16=bf16).reshape(M, topk, K)
+    ids = synthetic.expert_ids(M, E=E, topk=topk, seed=M + 60)
+    y = _run(wqs, qtype, N, K, x, ids)
+    ref, bnd = oracle.qmm_id(qtype, wqs, N, K, x, ids)
+    check_tol(y, ref, bnd, TOL_FP32, "%s per-slot M=%d" % (qtype, M))
+    # the broadcast form is the per-slot form with every slot given its token's row
+    xb = synthetic.activations(M, K, seed=M + 61, bf16=bf16)
+    y1 = _run(wqs, qtype, N, K, xb, ids)
+    y2 = _run(wqs, qtype, N, K, np.ascontiguousarray(np.repeat(xb[:, None, :], topk, axis=1)), ids)
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))

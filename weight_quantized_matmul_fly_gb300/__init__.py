@@ -11,10 +11,10 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["QmmError", "TYPES", "TYPE_ID", "X_BF16", "build", "lib", "qmm", "qmm_ws", "qmm_workspace_size",
+__all__ = ["QmmError", "TYPES", "TYPE_ID", "X_BF16", "X_PER_SLOT", "build", "lib", "qmm", "qmm_ws", "qmm_workspace_size",
            "qmm_launch_count", "qmm_noalloc", "NOALLOC_SCRATCH_BYTES",
            "qmm_id", "qmm_with_tile", "qmm_pick_tile", "qmm_pick_path", "qmm_dequant", "qmm_quantize",
-           "qmm_type_info", "qmm_get_status", "qmm_strerror", "row_bytes", "EXPORTS"]
+           "qmm_type_info", "qmm_get_status", "qmm_debug_stall", "qmm_strerror", "row_bytes", "EXPORTS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqmm.so")
@@ -23,12 +23,13 @@ TYPES = ["F32", "F16", "BF16", "Q4_0", "Q4_1", "Q5_0", "Q5_1", "Q8_0",
          "Q2_K", "Q3_K", "Q4_K", "Q5_K", "Q6_K", "A4G64"]
 TYPE_ID = {n: i for i, n in enumerate(TYPES)}
 X_BF16 = 0x100
+X_PER_SLOT = 0x200
 STATUS_BAD_ID, STATUS_TIMEOUT = 0x1, 0x2
 
 # Every symbol include/qmm.h declares.
 EXPORTS = ["qmm", "qmm_ws", "qmm_workspace_size", "qmm_noalloc", "qmm_id", "qmm_with_tile", "qmm_pick_tile",
            "qmm_pick_path", "qmm_launch_count", "qmm_dequant", "qmm_quantize", "qmm_type_info", "qmm_get_status",
-           "qmm_strerror"]
+           "qmm_debug_stall", "qmm_strerror"]
 NOALLOC_SCRATCH_BYTES = 64 << 20   # QMM_NOALLOC_SCRATCH_BYTES
 
 
@@ -67,7 +68,8 @@ def lib():
             "qmm_dequant": ([P, I, I64, I64, P, P], I),
             "qmm_quantize": ([P, I, I64, I64, P, P], I),
             "qmm_type_info": ([I, ctypes.POINTER(I), ctypes.POINTER(I)], I),
-            "qmm_get_status": ([P, ctypes.POINTER(ctypes.c_uint)], I),
+            "qmm_get_status": ([P], I),
+            "qmm_debug_stall": ([P, I, I64, I64, P, I64, P, P], I),
             "qmm_strerror": ([I], ctypes.c_char_p),
         }
         for name, (args, res) in sig.items():
@@ -174,10 +176,12 @@ def qmm_with_tile(wq, qtype, N: int, K: int, x, y, tile: int, stream=None):
 
 
 def qmm_id(wqs, qtype, N: int, K: int, x, ids, y, stream=None):
-    """y[M, topk, N]: for each token t and slot j, x[t] @ dequant(wqs[ids[t, j]])^T."""
+    """y[M, topk, N]: for each token t and slot j, x[t] @ dequant(wqs[ids[t, j]])^T; x of shape (M, K), or
+    (M, topk, K) for one activation row per (token, slot), which is then x[t, j]."""
     M, topk = ids.shape
+    flags = _xflag(x) | (X_PER_SLOT if x.dim() == 3 else 0)
     arr = (ctypes.c_void_p * len(wqs))(*[w.data_ptr() for w in wqs])
-    rc = lib().qmm_id(ctypes.cast(arr, ctypes.c_void_p), len(wqs), _qt(qtype) | _xflag(x), int(N), int(K),
+    rc = lib().qmm_id(ctypes.cast(arr, ctypes.c_void_p), len(wqs), _qt(qtype) | flags, int(N), int(K),
                       _ptr(x), _ptr(ids), int(M), int(topk), _ptr(y), _stream(stream))
     _check(rc, "qmm_id")
     return y
@@ -195,6 +199,17 @@ def qmm_quantize(w_in, qtype, N: int, K: int, wq_out, stream=None):
 
 
 def qmm_get_status(stream=None) -> int:
-    v = ctypes.c_uint(0)
-    _check(lib().qmm_get_status(_stream(stream), ctypes.byref(v)), "qmm_get_status")
-    return v.value
+    """The device status bits (QMM_STATUS_*) since the last call, read and cleared (synchronises)."""
+    rc = lib().qmm_get_status(_stream(stream))
+    if rc < 0:
+        raise QmmError(rc, "qmm_get_status")
+    return rc
+
+
+def qmm_debug_stall(wq, qtype, N: int, K: int, x, y, stream=None):
+    """Test hook: a mat-vec call in which one bounded wait is made to run out (see include/qmm.h)."""
+    M = x.shape[0]
+    rc = lib().qmm_debug_stall(_ptr(wq), _qt(qtype) | _xflag(x), int(N), int(K), _ptr(x), int(M), _ptr(y),
+                               _stream(stream))
+    _check(rc, "qmm_debug_stall")
+    return y

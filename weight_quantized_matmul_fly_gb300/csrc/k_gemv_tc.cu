@@ -385,7 +385,9 @@ template <int NT, bool XBF16> struct Layout {
     static constexpr int COLS = 8 * NT;              // MMA columns
     static constexpr int TOK = XBF16 ? 8 * NT : 4 * NT;   // tokens served
     static constexpr int WARPS = 8;
-    static constexpr int BARS = WARPS * NSMAX * 8;
+    // the warps' stage barriers, then one barrier that is initialised but never signalled (a test hook
+    // waits on it to make a bounded wait run out)
+    static constexpr int BARS = WARPS * NSMAX * 8 + 16;
     __host__ __device__ static int xs_stride(int kpad) { return kpad + 16; }   // elements; +32 B breaks bank aliasing
     // Columns actually staged: with one column group only those the tokens use (a power of two; the MMA
     // reads the others from a used column and their results are never read).
@@ -517,7 +519,7 @@ __device__ __forceinline__ void macro_step(const typename Frag<QT>::Raw &cur0, c
 template <int QT, int NT, bool XBF16, int KW>
 __global__ void __launch_bounds__(256, 2)
     gemv_tc_kernel(const uint8_t *__restrict__ wq, int N, int64_t K, int64_t rowbytes, const void *__restrict__ x,
-                   int M, float *__restrict__ y, int kseg, int ns, unsigned int *__restrict__ status) {
+                   int M, float *__restrict__ y, int kseg, int ns, unsigned int *__restrict__ status, int stall) {
     using F = Frag<QT>;
     using LY = Layout<NT, XBF16>;
     constexpr int WARPS = LY::WARPS, RG = WARPS / KW;
@@ -586,6 +588,13 @@ __global__ void __launch_bounds__(256, 2)
     const uintptr_t radr0 = reinterpret_cast<uintptr_t>(wq + (int64_t)(nrow0 + g < N ? nrow0 + g : N - 1) * rowbytes);
     const uintptr_t radr1 =
         reinterpret_cast<uintptr_t>(wq + (int64_t)(nrow0 + g + 8 < N ? nrow0 + g + 8 : N - 1) * rowbytes);
+
+    // Test hook (stall != 0): every warp of the first CTA that has weights to decode waits for its first
+    // weight stage on `never`, a barrier nobody arrives on, so that the bounded wait runs out; the copies
+    // themselves are issued and waited for (drained) as usual.
+    uint64_t *never = bars + WARPS * NSMAX;
+    const bool stall_here = stall != 0 && blockIdx.x == 0 && blockIdx.y == 0;
+    if (stall_here && warp == 0 && lane == 0) ptx::mbar_init(never, 1);   // visible after the staging barrier
 
     // The weights are requested before waiting for the preceding kernel in the stream (they are model data
     // that no kernel of this library writes); activations and outputs are touched only after.
@@ -696,15 +705,18 @@ __global__ void __launch_bounds__(256, 2)
     for (; done < nsteps; ++done) {
         const int64_t mb = mb_beg + done;
         const uint8_t *p0, *p1;
+        uint64_t *first = stall_here && done == 0 ? never : nullptr;
         if (resident) {
-            if (done == 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(gbar, 0u, status))) break;
+            if (done == 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(first ? first : gbar, 0u, status))) break;
             const uintptr_t so = (uintptr_t)(smb * BPM * BYTES);          // the segment's first byte in a row
             const size_t jo = (size_t)(mb - smb) * BPM * BYTES;           // this macro block within the segment
             p0 = gtile + (size_t)g * rstride + ((radr0 + so) & 15) + jo;
             p1 = gtile + (size_t)(g + 8) * rstride + ((radr1 + so) & 15) + jo;
         } else {
             const int slot = done % ns;
-            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&wbar[slot], (uint32_t)((done / ns) & 1), status))) break;
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(first ? first : &wbar[slot], (uint32_t)((done / ns) & 1),
+                                                         status)))
+                break;
             const uintptr_t mo = (uintptr_t)(mb * BPM * BYTES);
             p0 = wring + (size_t)(slot * 16 + g) * SLOT + ((radr0 + mo) & 15);
             p1 = wring + (size_t)(slot * 16 + g + 8) * SLOT + ((radr1 + mo) & 15);
@@ -723,10 +735,17 @@ __global__ void __launch_bounds__(256, 2)
             if (done + ns < nsteps) issue(done + ns);
         }
     }
-    // After a timeout: wait (bounded) for the copies still in flight before the shared memory is released.
-    if (!resident)
-        for (int i = done + 1; i < nsteps && i < done + ns; ++i)
-            ptx::mbar_wait(&wbar[i % ns], (uint32_t)((i / ns) & 1), status);
+    // After a timeout: wait (bounded) for this warp's copies still in flight before the shared memory is
+    // released: in the ring, the stage that was being waited for and those issued after it; in resident
+    // mode, the tile (its copies were issued by this row group's first warp).
+    if (done < nsteps) {
+        if (resident) {
+            if (done == 0) ptx::mbar_wait(gbar, 0u, status);
+        } else {
+            for (int i = done; i < nsteps && i < done + ns; ++i)
+                ptx::mbar_wait(&wbar[i % ns], (uint32_t)((i / ns) & 1), status);
+        }
+    }
 
     // ---- results. binary32 x: acc[mt][0] = (row g, token 4mt+t), acc[mt][2] = (row g+8, token 4mt+t);
     //      bf16 x: acc[mt][0/1] = (row g, tokens 8mt+2t, +1), acc[mt][2/3] = (row g+8, same tokens).
@@ -801,7 +820,7 @@ struct IdExperts {
 template <int QT, int NT, bool XBF16, int KW>
 __global__ void __launch_bounds__(256, 2)
     gemv_tc_id_kernel(const __grid_constant__ IdExperts ex, int E, int N, int64_t K, int64_t rowbytes,
-                      const void *__restrict__ x, const int32_t *__restrict__ ids, int M, int topk,
+                      const void *__restrict__ x, int xdiv, const int32_t *__restrict__ ids, int M, int topk,
                       float *__restrict__ y, int kseg, unsigned int *__restrict__ status) {
     using F = Frag<QT>;
     using LY = Layout<NT, XBF16>;
@@ -946,7 +965,7 @@ __global__ void __launch_bounds__(256, 2)
             for (int idx = tid; idx < total; idx += WARPS * 32) {
                 const int tk = idx / k4n, k4 = idx - tk * k4n;
                 const int64_t k = kb + 4 * k4;
-                const int tok = s_slot[p0 + tk] / topk;
+                const int tok = s_slot[p0 + tk] / xdiv;     // x row: the token's (xdiv = topk) or the slot's
                 float v[4] = {0.f, 0.f, 0.f, 0.f};
                 if (k < ke) {
                     if constexpr (XBF16) {
@@ -1120,7 +1139,7 @@ int64_t gtc_capacity(int64_t S, size_t smem) {
 
 template <int QT, int NT, bool XBF16, int KW>
 int launch_gtc_kw(const void *wq, int64_t N, int64_t K, const void *x, int M, float *y, int64_t S, int64_t kseg,
-                  int ns, unsigned int *status, cudaStream_t st) {
+                  int ns, unsigned int *status, cudaStream_t st, int stall) {
     using LY = gtc::Layout<NT, XBF16>;
     constexpr int UNIT = gtc::Frag<QT>::UNIT, RG = LY::WARPS / KW;
     auto kern = gtc::gemv_tc_kernel<QT, NT, XBF16, KW>;
@@ -1144,7 +1163,7 @@ int launch_gtc_kw(const void *wq, int64_t N, int64_t K, const void *x, int M, fl
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t *>(wq), (int)N, K, row_bytes(QT, K), x,
-                                       M, y, (int)kseg, ns, status);
+                                       M, y, (int)kseg, ns, status, stall);
     return e == cudaSuccess ? 0 : -6;
 }
 
@@ -1157,7 +1176,7 @@ int launch_gtc_kw(const void *wq, int64_t N, int64_t K, const void *x, int M, fl
 // warp's ring takes as many stages as the shared memory left over allows (at most its macro blocks).
 template <int QT, int NT, bool XBF16>
 int launch_gtc_t(const void *wq, int64_t N, int64_t K, const void *x, int M, float *y, unsigned int *status,
-                 cudaStream_t st, bool dry) {
+                 cudaStream_t st, bool dry, int stall) {
     using LY = gtc::Layout<NT, XBF16>;
     constexpr int UNIT = gtc::Frag<QT>::UNIT, SLOT = gtc::slot_bytes<QT>();
     constexpr int MB_BYTES = 256 / TypeInfo<QT>::QK * TypeInfo<QT>::BYTES;   // bytes of a macro block
@@ -1219,10 +1238,10 @@ int launch_gtc_t(const void *wq, int64_t N, int64_t K, const void *x, int M, flo
     if (NT > 1 && best_ns > 0 && N * row_bytes(QT, K) < ((int64_t)64 << 20)) return -3;
     if (dry) return 0;                                                // planning only (launch counting)
     const int64_t kseg = ((nmacro + best_s - 1) / best_s) * 256;
-    if constexpr (KWMAX >= 8) if (best_kw == 8) return launch_gtc_kw<QT, NT, XBF16, 8>(wq, N, K, x, M, y, best_s, kseg, best_ns, status, st);
-    if constexpr (KWMAX >= 4) if (best_kw == 4) return launch_gtc_kw<QT, NT, XBF16, 4>(wq, N, K, x, M, y, best_s, kseg, best_ns, status, st);
-    if constexpr (KWMAX >= 2) if (best_kw == 2) return launch_gtc_kw<QT, NT, XBF16, 2>(wq, N, K, x, M, y, best_s, kseg, best_ns, status, st);
-    return launch_gtc_kw<QT, NT, XBF16, 1>(wq, N, K, x, M, y, best_s, kseg, best_ns, status, st);
+    if constexpr (KWMAX >= 8) if (best_kw == 8) return launch_gtc_kw<QT, NT, XBF16, 8>(wq, N, K, x, M, y, best_s, kseg, best_ns, status, st, stall);
+    if constexpr (KWMAX >= 4) if (best_kw == 4) return launch_gtc_kw<QT, NT, XBF16, 4>(wq, N, K, x, M, y, best_s, kseg, best_ns, status, st, stall);
+    if constexpr (KWMAX >= 2) if (best_kw == 2) return launch_gtc_kw<QT, NT, XBF16, 2>(wq, N, K, x, M, y, best_s, kseg, best_ns, status, st, stall);
+    return launch_gtc_kw<QT, NT, XBF16, 1>(wq, N, K, x, M, y, best_s, kseg, best_ns, status, st, stall);
 }
 
 struct GtcLaunch {
@@ -1235,23 +1254,24 @@ struct GtcLaunch {
     unsigned int *status;
     cudaStream_t st;
     bool dry;
+    int stall;
     template <int QT> int operator()() {
         if constexpr (QT <= T_BF16) {
             return -1;
         } else {
-            if (xbf16) return M <= 8 ? launch_gtc_t<QT, 1, true>(wq, N, K, x, M, y, status, st, dry)
-                                     : launch_gtc_t<QT, 2, true>(wq, N, K, x, M, y, status, st, dry);
-            if (M <= 4) return launch_gtc_t<QT, 1, false>(wq, N, K, x, M, y, status, st, dry);
-            if (M <= 8) return launch_gtc_t<QT, 2, false>(wq, N, K, x, M, y, status, st, dry);
-            return launch_gtc_t<QT, 4, false>(wq, N, K, x, M, y, status, st, dry);
+            if (xbf16) return M <= 8 ? launch_gtc_t<QT, 1, true>(wq, N, K, x, M, y, status, st, dry, stall)
+                                     : launch_gtc_t<QT, 2, true>(wq, N, K, x, M, y, status, st, dry, stall);
+            if (M <= 4) return launch_gtc_t<QT, 1, false>(wq, N, K, x, M, y, status, st, dry, stall);
+            if (M <= 8) return launch_gtc_t<QT, 2, false>(wq, N, K, x, M, y, status, st, dry, stall);
+            return launch_gtc_t<QT, 4, false>(wq, N, K, x, M, y, status, st, dry, stall);
         }
     }
 };
 
 // ---- expert-indexed launches
 template <int QT, int NT, bool XBF16, int KW>
-int launch_gtc_id_kw(const gtc::IdExperts &ex, int E, int64_t N, int64_t K, const void *x, const int32_t *ids, int M,
-                     int topk, float *y, int S, int64_t kseg, size_t smem, unsigned int *status, cudaStream_t st) {
+int launch_gtc_id_kw(const gtc::IdExperts &ex, int E, int64_t N, int64_t K, const void *x, int xdiv, const int32_t *ids,
+                     int M, int topk, float *y, int S, int64_t kseg, size_t smem, unsigned int *status, cudaStream_t st) {
     using LY = gtc::Layout<NT, XBF16>;
     constexpr int RG = LY::WARPS / KW;
     auto kern = gtc::gemv_tc_id_kernel<QT, NT, XBF16, KW>;
@@ -1277,8 +1297,8 @@ int launch_gtc_id_kw(const gtc::IdExperts &ex, int E, int64_t N, int64_t K, cons
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ex, E, (int)N, K, row_bytes(QT, K), x, ids, M, topk, y, (int)kseg,
-                                       status);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ex, E, (int)N, K, row_bytes(QT, K), x, xdiv, ids, M, topk, y,
+                                       (int)kseg, status);
     return e == cudaSuccess ? 0 : -6;
 }
 
@@ -1287,8 +1307,8 @@ int launch_gtc_id_kw(const gtc::IdExperts &ex, int E, int64_t N, int64_t K, cons
 // blocks per warp + a per-CTA prologue), over CTAs of every possible expert (those of absent experts leave
 // at once), with the whole row-block tile resident in shared memory. Returns -3 when no split fits.
 template <int QT, int NT, bool XBF16>
-int launch_gtc_id_t(const gtc::IdExperts &ex, int E, int64_t N, int64_t K, const void *x, const int32_t *ids, int M,
-                    int topk, float *y, unsigned int *status, cudaStream_t st) {
+int launch_gtc_id_t(const gtc::IdExperts &ex, int E, int64_t N, int64_t K, const void *x, int xdiv, const int32_t *ids,
+                    int M, int topk, float *y, unsigned int *status, cudaStream_t st) {
     using LY = gtc::Layout<NT, XBF16>;
     constexpr int UNIT = gtc::Frag<QT>::UNIT, TOK = LY::TOK;
     constexpr int MB_BYTES = 256 / TypeInfo<QT>::QK * TypeInfo<QT>::BYTES;
@@ -1323,10 +1343,10 @@ int launch_gtc_id_t(const gtc::IdExperts &ex, int E, int64_t N, int64_t K, const
     }
     if (best_cost < 0) return -3;
     const int64_t kseg = ((nmacro + best_s - 1) / best_s) * 256;
-    if constexpr (KWMAX >= 8) if (best_kw == 8) return launch_gtc_id_kw<QT, NT, XBF16, 8>(ex, E, N, K, x, ids, M, topk, y, best_s, kseg, best_smem, status, st);
-    if constexpr (KWMAX >= 4) if (best_kw == 4) return launch_gtc_id_kw<QT, NT, XBF16, 4>(ex, E, N, K, x, ids, M, topk, y, best_s, kseg, best_smem, status, st);
-    if constexpr (KWMAX >= 2) if (best_kw == 2) return launch_gtc_id_kw<QT, NT, XBF16, 2>(ex, E, N, K, x, ids, M, topk, y, best_s, kseg, best_smem, status, st);
-    return launch_gtc_id_kw<QT, NT, XBF16, 1>(ex, E, N, K, x, ids, M, topk, y, best_s, kseg, best_smem, status, st);
+    if constexpr (KWMAX >= 8) if (best_kw == 8) return launch_gtc_id_kw<QT, NT, XBF16, 8>(ex, E, N, K, x, xdiv, ids, M, topk, y, best_s, kseg, best_smem, status, st);
+    if constexpr (KWMAX >= 4) if (best_kw == 4) return launch_gtc_id_kw<QT, NT, XBF16, 4>(ex, E, N, K, x, xdiv, ids, M, topk, y, best_s, kseg, best_smem, status, st);
+    if constexpr (KWMAX >= 2) if (best_kw == 2) return launch_gtc_id_kw<QT, NT, XBF16, 2>(ex, E, N, K, x, xdiv, ids, M, topk, y, best_s, kseg, best_smem, status, st);
+    return launch_gtc_id_kw<QT, NT, XBF16, 1>(ex, E, N, K, x, xdiv, ids, M, topk, y, best_s, kseg, best_smem, status, st);
 }
 
 struct GtcIdLaunch {
@@ -1335,6 +1355,7 @@ struct GtcIdLaunch {
     int E;
     int64_t N, K;
     const void *x;
+    int xdiv;
     const int32_t *ids;
     int M, topk;
     float *y;
@@ -1345,8 +1366,8 @@ struct GtcIdLaunch {
             return -3;
         } else {
             // one 4-token (8 for bf16 activations) column group per pass: an expert rarely gets more
-            if (xbf16) return launch_gtc_id_t<QT, 1, true>(*ex, E, N, K, x, ids, M, topk, y, status, st);
-            return launch_gtc_id_t<QT, 1, false>(*ex, E, N, K, x, ids, M, topk, y, status, st);
+            if (xbf16) return launch_gtc_id_t<QT, 1, true>(*ex, E, N, K, x, xdiv, ids, M, topk, y, status, st);
+            return launch_gtc_id_t<QT, 1, false>(*ex, E, N, K, x, xdiv, ids, M, topk, y, status, st);
         }
     }
 };
@@ -1357,18 +1378,19 @@ struct GtcIdLaunch {
 // cluster allows cannot hold the activations of this many tokens (the caller then halves the group).
 // dry: plan only, launch nothing (0 or -3), for counting launches.
 int launch_gemv_tc(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int M, float *y,
-                   unsigned int *status, cudaStream_t st, bool dry) {
-    GtcLaunch f{xbf16, wq, N, K, x, M, y, status, st, dry};
+                   unsigned int *status, cudaStream_t st, bool dry, int stall) {
+    GtcLaunch f{xbf16, wq, N, K, x, M, y, status, st, dry, stall};
     return dispatch_type(qt, f);
 }
 
 // Expert-indexed product on the tensor-core mat-vec machinery (quantized types). Returns -3 when it does
 // not apply (plain types, or no work split fits on chip); the caller then uses the CUDA-core kernel.
 int launch_gemv_tc_id(int qt, bool xbf16, const void *const *wq, int64_t E, int64_t N, int64_t K, const void *x,
-                      const int32_t *ids, int64_t M, int topk, float *y, unsigned int *status, cudaStream_t st) {
+                      bool x_per_slot, const int32_t *ids, int64_t M, int topk, float *y, unsigned int *status,
+                      cudaStream_t st) {
     gtc::IdExperts ex;
     for (int e = 0; e < QMM_MAX_EXPERTS; ++e) ex.p[e] = e < E ? static_cast<const uint8_t *>(wq[e]) : nullptr;
-    GtcIdLaunch f{xbf16, &ex, (int)E, N, K, x, ids, (int)M, topk, y, status, st};
+    GtcIdLaunch f{xbf16, &ex, (int)E, N, K, x, x_per_slot ? 1 : topk, ids, (int)M, topk, y, status, st};
     return dispatch_type(qt, f);
 }
 

@@ -394,7 +394,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 1) ptx::tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == 1) {
+        // every MMA this CTA issued has completed before its accumulator is freed, also when a bounded
+        // wait gave up above (the issuer committed `done` after its last MMA whatever happened)
+        if (nsteps > 0) {
+            if (lane == 0) ptx::mbar_wait(&sm->done, 0, status);
+            __syncwarp();
+            ptx::tc_fence_after();
+        }
+        ptx::tmem_dealloc(tmem, TMEM_COLS);
+    }
 }
 
 // y[i] = sum over s of part[s][i], s ascending (deterministic K-split reduction).

@@ -55,8 +55,8 @@ __device__ __forceinline__ void load_x32(const void *x, int64_t off, float (&v)[
 template <int QT, bool XBF16>
 __global__ void __launch_bounds__(WARPS * 32)
     mvid_kernel(const __grid_constant__ Experts ex, int E, int64_t N, int64_t K, int64_t rowbytes,
-                const void *__restrict__ x, const int32_t *__restrict__ ids, int M, int topk, float *__restrict__ y,
-                int split, unsigned int *status) {
+                const void *__restrict__ x, int xdiv, const int32_t *__restrict__ ids, int M, int topk,
+                float *__restrict__ y, int split, unsigned int *status) {
     __shared__ int s_ids[QMM_MAX_ID_SLOTS];
     __shared__ int s_slots[QMM_MAX_ID_SLOTS];   // slots routed to this CTA's expert, ascending
     __shared__ int s_rank[QMM_MAX_EXPERTS];
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(WARPS * 32)
 #pragma unroll
                     for (int j = 0; j < TOKG; ++j) {
                         if (t0 + j < ns) {
-                            const int tok = s_slots[t0 + j] / topk;
+                            const int tok = s_slots[t0 + j] / xdiv;   // the token's row, or the slot's
                             float xv[32];
                             load_x32<XBF16>(x, (int64_t)tok * K + 32 * (int64_t)c, xv);
                             float s = acc[j];
@@ -172,6 +172,7 @@ struct MvidLaunch {
     int E;
     int64_t N, K;
     const void *x;
+    int xdiv;
     const int32_t *ids;
     int M, topk;
     float *y;
@@ -182,18 +183,19 @@ struct MvidLaunch {
     template <int QT> int operator()() {
         const int64_t rb = row_bytes(QT, K);
         if (xbf16)
-            mvid::mvid_kernel<QT, true><<<grid, mvid::WARPS * 32, 0, st>>>(*ex, E, N, K, rb, x, ids, M, topk, y,
-                                                                          split, status);
+            mvid::mvid_kernel<QT, true><<<grid, mvid::WARPS * 32, 0, st>>>(*ex, E, N, K, rb, x, xdiv, ids, M, topk,
+                                                                          y, split, status);
         else
-            mvid::mvid_kernel<QT, false><<<grid, mvid::WARPS * 32, 0, st>>>(*ex, E, N, K, rb, x, ids, M, topk, y,
-                                                                           split, status);
+            mvid::mvid_kernel<QT, false><<<grid, mvid::WARPS * 32, 0, st>>>(*ex, E, N, K, rb, x, xdiv, ids, M,
+                                                                           topk, y, split, status);
         return cudaGetLastError() == cudaSuccess ? 0 : -6;
     }
 };
 }  // namespace
 
 int launch_mvid(int qt, bool xbf16, const void *const *wq, int64_t E, int64_t N, int64_t K, const void *x,
-                const int32_t *ids, int64_t M, int topk, float *y, unsigned int *status, cudaStream_t st) {
+                bool x_per_slot, const int32_t *ids, int64_t M, int topk, float *y, unsigned int *status,
+                cudaStream_t st) {
     mvid::Experts ex;
     for (int e = 0; e < QMM_MAX_EXPERTS; ++e) ex.p[e] = e < E ? static_cast<const uint8_t *>(wq[e]) : nullptr;
     const int64_t nb32 = K / 32;
@@ -201,7 +203,7 @@ int launch_mvid(int qt, bool xbf16, const void *const *wq, int64_t E, int64_t N,
     const int64_t slots = M * topk;
     const int64_t maxexp = slots < E ? slots : E;
     dim3 grid((unsigned)((N + mvid::ROWS_PER_CTA - 1) / mvid::ROWS_PER_CTA), (unsigned)maxexp);
-    MvidLaunch f{xbf16, &ex, (int)E, N, K, x, ids, (int)M, topk, y, split, grid, status, st};
+    MvidLaunch f{xbf16, &ex, (int)E, N, K, x, x_per_slot ? 1 : topk, ids, (int)M, topk, y, split, grid, status, st};
     return dispatch_type(qt, f);
 }
 

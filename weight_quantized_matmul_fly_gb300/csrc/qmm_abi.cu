@@ -13,16 +13,18 @@ __device__ unsigned int g_status = 0;
 int launch_gemv(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int64_t M, float *y,
                 cudaStream_t st);
 int launch_gemv_tc(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int M, float *y,
-                   unsigned int *status, cudaStream_t st, bool dry = false);
+                   unsigned int *status, cudaStream_t st, bool dry = false, int stall = 0);
 int launch_gemv_tc_id(int qt, bool xbf16, const void *const *wq, int64_t E, int64_t N, int64_t K, const void *x,
-                      const int32_t *ids, int64_t M, int topk, float *y, unsigned int *status, cudaStream_t st);
+                      bool x_per_slot, const int32_t *ids, int64_t M, int topk, float *y, unsigned int *status,
+                      cudaStream_t st);
 int launch_mm(int qt, int tile, const void *wq, int64_t N, int64_t K, const void *x_bf16, int64_t M, float *y,
               float *part, unsigned int *status, cudaStream_t st);
 size_t mm_partial_bytes(int qt, int64_t N, int64_t K, int64_t M);
 int mm_ksplit(int qt, int64_t N, int64_t K, int64_t M);
 int launch_x_to_bf16(const float *x, void *out, int64_t n, cudaStream_t st);
 int launch_mvid(int qt, bool xbf16, const void *const *wq, int64_t E, int64_t N, int64_t K, const void *x,
-                const int32_t *ids, int64_t M, int topk, float *y, unsigned int *status, cudaStream_t st);
+                bool x_per_slot, const int32_t *ids, int64_t M, int topk, float *y, unsigned int *status,
+                cudaStream_t st);
 int launch_dequant(int qt, const void *wq, int64_t N, int64_t K, float *out, cudaStream_t st);
 int launch_quantize(int qt, const float *w, int64_t N, int64_t K, void *out, cudaStream_t st);
 }  // namespace wqk
@@ -69,7 +71,7 @@ unsigned int *status_ptr() {
 // halved when the activations of a K segment would not fit on chip); the plain types on the binary32 one.
 // With `launches` non-null nothing is launched: the launches the call would make are counted instead.
 int run_matvec(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int64_t M, float *y,
-               cudaStream_t st, int *launches = nullptr) {
+               cudaStream_t st, int *launches = nullptr, int stall = 0) {
     if (is_plain(qt)) {
         if (launches) { *launches = (int)((M + 15) / 16); return 0; }
         return launch_gemv(qt, xbf16, wq, N, K, x, M, y, st);
@@ -83,7 +85,7 @@ int run_matvec(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const v
         int rc;
         for (;;) {
             rc = launch_gemv_tc(qt, xbf16, wq, N, K, static_cast<const uint8_t *>(x) + m0 * K * esz, mg,
-                                y + m0 * N, status, st, launches != nullptr);
+                                y + m0 * N, status, st, launches != nullptr, m0 == 0 ? stall : 0);
             if (rc != -3 || mg <= 4) break;
             mg = (mg + 1) / 2;
         }
@@ -198,7 +200,7 @@ int qmm_with_tile(const void *wq, int qtype, int64_t N, int64_t K, const void *x
 
 int qmm_id(const void *const *wq, int64_t E, int qtype, int64_t N, int64_t K, const void *x, const int32_t *ids,
            int64_t M, int topk, float *y, void *stream) {
-    if ((qtype & ~(0xff | QMM_X_BF16)) != 0) return QMM_EQTYPE;
+    if ((qtype & ~(0xff | QMM_X_BF16 | QMM_X_PER_SLOT)) != 0) return QMM_EQTYPE;
     const int qt = qtype & 0xff;
     if (qt < 0 || qt >= T_COUNT) return QMM_EQTYPE;
     if (N <= 0 || K <= 0 || M <= 0 || N >= kMaxDim || K >= kMaxDim) return QMM_EDIM;
@@ -212,10 +214,11 @@ int qmm_id(const void *const *wq, int64_t E, int qtype, int64_t N, int64_t K, co
     if (!aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(ids) & 3u)) return QMM_EALIGN;
     unsigned int *status = status_ptr();
     if (!status) return QMM_ECUDA;
-    const int rc = launch_gemv_tc_id(qt, (qtype & QMM_X_BF16) != 0, wq, E, N, K, x, ids, M, topk, y, status,
+    const bool xbf16 = (qtype & QMM_X_BF16) != 0, per_slot = (qtype & QMM_X_PER_SLOT) != 0;
+    const int rc = launch_gemv_tc_id(qt, xbf16, wq, E, N, K, x, per_slot, ids, M, topk, y, status,
                                      static_cast<cudaStream_t>(stream));
     if (rc != -3) return rc;
-    return launch_mvid(qt, (qtype & QMM_X_BF16) != 0, wq, E, N, K, x, ids, M, topk, y, status,
+    return launch_mvid(qt, xbf16, wq, E, N, K, x, per_slot, ids, M, topk, y, status,
                        static_cast<cudaStream_t>(stream));
 }
 
@@ -245,8 +248,7 @@ int qmm_type_info(int qtype, int *block_weights, int *block_bytes) {
     return 0;
 }
 
-int qmm_get_status(void *stream, unsigned int *status) {
-    if (!status) return QMM_ENULL;
+int qmm_get_status(void *stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     unsigned int zero = 0, v = 0;
     if (cudaMemcpyFromSymbolAsync(&v, g_status, sizeof(v), 0, cudaMemcpyDeviceToHost, st) != cudaSuccess)
@@ -254,8 +256,17 @@ int qmm_get_status(void *stream, unsigned int *status) {
     if (cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st) != cudaSuccess)
         return QMM_ECUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return QMM_ECUDA;
-    *status = v;
-    return 0;
+    return (int)(v & 0x7fffffffu);
+}
+
+int qmm_debug_stall(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, float *y,
+                    void *stream) {
+    int rc = check_qmm(wq, qtype, N, K, x, M, y);
+    if (rc) return rc;
+    const int qt = qtype & 0xff;
+    if (is_plain(qt) || M > kGemvMaxM) return QMM_ERANGE;
+    return run_matvec(qt, (qtype & QMM_X_BF16) != 0, wq, N, K, x, M, y, static_cast<cudaStream_t>(stream),
+                      nullptr, 1);
 }
 
 int qmm_launch_count(int qtype, int64_t N, int64_t K, int64_t M) {

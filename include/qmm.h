@@ -90,19 +90,27 @@ enum qmm_type {
  * path rounds x and the dequantized weights to bfloat16 (round to nearest even) and accumulates in
  * binary32 (for Q4_K, Q5_K and A4G64 the weight rounded is the binary32 weight up to 2^-17 times its
  * sub-block scale); the mat-vec path multiplies the binary32 dequantized weights by x in binary32.
- * The tensor-core path needs device scratch: M*K*2 bytes for the bfloat16 copy of binary32 x, and, when
- * its work plan (a function of the type, N, K and M) splits the K dimension over S CTAs, S*M*N*4 bytes of
- * binary32 partial sums (added in a fixed order by a second kernel). qmm() takes the scratch from the stream-ordered
- * allocator (cudaMallocAsync / cudaFreeAsync on `stream`); callers that manage memory themselves use
- * qmm_ws() with qmm_workspace_size() bytes.
+ * qmm() allocates nothing and launches one kernel per call on either path. Its work plan (a function of
+ * the type, N, K and M) may split the K dimension over S <= 8 thread blocks; they form a cluster and add
+ * their partial sums in split order in shared memory. Binary32 activations are rounded to bfloat16 inside
+ * the tensor-core kernel, with at most 128 token columns per thread block. qmm_ws() is faster on that
+ * path with binary32 activations and M > 32: with scratch (qmm_workspace_size()), a separate pass writes a
+ * bfloat16 copy of x that the kernel reads at the plan's full width, and a K split (up to 32 thread blocks)
+ * sends its partial sums through the scratch to a second kernel that adds them in split order. The two
+ * plan their K split separately, so their results can differ in the last bits (both within the stated
+ * tolerance); each is bit-identical across token tiles.
  */
 int qmm(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, float *y, void *stream);
 
-/* Bytes of scratch qmm_ws() needs for these arguments (0 when none). */
+/* Bytes of scratch qmm_ws() needs for these arguments (0 when none): on the tensor-core path with binary32
+ * x and M > 32, M*K*2 bytes (rounded up to 256) for its bfloat16 copy plus S*M*N*4 bytes for the partial sums
+ * when the plan splits K over S thread blocks; nothing on the mat-vec path, up to 32 tokens, or with
+ * bfloat16 activations (qmm_ws then runs as qmm). */
 size_t qmm_workspace_size(int qtype, int64_t N, int64_t K, int64_t M);
 
 /* qmm() with caller-provided scratch: `workspace` is a device buffer of at least
- * qmm_workspace_size(...) bytes, 256-byte aligned; may be NULL when that size is 0. */
+ * qmm_workspace_size(...) bytes, 256-byte aligned; may be NULL when that size is 0 (QMM_EWORKSPACE when
+ * the size is not 0 and the buffer is missing or smaller). */
 int qmm_ws(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, float *y,
            void *workspace, size_t workspace_bytes, void *stream);
 
@@ -170,9 +178,16 @@ int qmm_pick_tile(int64_t M);
 /* Which path qmm() takes for M tokens: 0 = mat-vec, 32/64/128 = tensor-core tile. */
 int qmm_pick_path(int qtype, int64_t N, int64_t K, int64_t M);
 
-/* How many kernels one qmm() / qmm_ws() call with these arguments launches (diagnostic). The mat-vec path
- * is planned as the call would plan it (token groups of 16, halved where their activations do not fit on
- * chip), which needs the current device; without one it assumes one launch per 16 tokens. */
+/* The tensor-core work plan a qmm_ws() call with its workspace uses (diagnostic): the K split and the token
+ * columns per thread block (before the cap at 128 that binary32 activations converted in the kernel get).
+ * Returns the path as qmm_pick_path() does; on the mat-vec path (0) both outputs are 0. Without a device
+ * the plan assumes unconstrained cluster packing. */
+int qmm_plan_info(int qtype, int64_t N, int64_t K, int64_t M, int *ksplit, int *cols);
+
+/* How many kernels one qmm_ws() call with these arguments and its workspace launches (diagnostic; qmm()
+ * launches one kernel on the tensor-core path). The mat-vec path is planned as the call would plan it
+ * (token groups of 16, halved where their activations do not fit on chip), which needs the current
+ * device; without one it assumes one launch per 16 tokens. */
 int qmm_launch_count(int qtype, int64_t N, int64_t K, int64_t M);
 
 /*

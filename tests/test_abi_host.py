@@ -114,17 +114,26 @@ def test_pick_path(L):
 def test_workspace_size(L):
     # the mat-vec path needs no scratch
     assert qmm.qmm_workspace_size("Q4_K", 4096, 2560, 1) == 0
-    # tensor-core path: a bf16 copy of binary32 activations ...
+    # tensor-core path with binary32 x: its bf16 copy (and the partial sums of a K split) ...
     assert qmm.qmm_workspace_size("Q4_K", 9728, 2560, 2048) >= 2048 * 2560 * 2
+    ws = qmm.qmm_workspace_size("Q4_K", 1024, 2560, 100)
+    assert qmm.qmm_plan_info("Q4_K", 1024, 2560, 100)[1] > 1 and ws >= 100 * 2560 * 2 + 2 * 100 * 1024 * 4
+    # up to 32 tokens the kernel converts x itself (measured as fast as the copy there)
+    assert qmm.qmm_workspace_size("Q4_K", 1024, 2560, 32) == 0
+    # ... and nothing with bf16 x (a K split is added inside a cluster)
     assert qmm.qmm_workspace_size("Q4_K", 9728, 2560, 2048, x_bf16=True) == 0
-    # ... plus binary32 partials when few row blocks make the K dimension split over CTAs
-    fp32 = qmm.qmm_workspace_size("Q4_K", 1024, 2560, 100)
-    bf16 = qmm.qmm_workspace_size("Q4_K", 1024, 2560, 100, x_bf16=True)
-    assert bf16 >= 2 * 100 * 1024 * 4 and fp32 >= bf16 + 100 * 2560 * 2
+    assert qmm.qmm_workspace_size("Q6_K", 1024, 2560, 33, x_bf16=True) == 0
 
 
 def test_launch_count(L):
     assert qmm.qmm_launch_count("Q4_K", 9728, 2560, 1) == 1
-    assert qmm.qmm_launch_count("Q4_K", 9728, 2560, 2048) == 2            # bf16 copy of x + mm
+    assert qmm.qmm_launch_count("Q4_K", 9728, 2560, 2048) == 2            # bf16 copy of x + mm (qmm_ws)
     assert qmm.qmm_launch_count("Q4_K", 9728, 2560, 2048, x_bf16=True) == 1
-    assert qmm.qmm_launch_count("Q4_K", 1024, 2560, 100) == 3             # + split-K reduction
+    assert qmm.qmm_launch_count("Q4_K", 1024, 2560, 100, x_bf16=True) == 1   # K split inside a cluster
+    assert qmm.qmm_launch_count("Q4_K", 1024, 2560, 100) == 3             # copy of x + mm + split reduction
+
+
+def test_noalloc_checks_arguments_first(L):
+    # a null x with a large M is a null pointer, not an oversized workspace
+    assert L.qmm_noalloc(P(A), 3, 64, 8192, None, 1 << 20, P(A), None) == -4
+    assert L.qmm_noalloc(P(A), 3, 64, -64, P(A), 1 << 20, P(A), None) == -3

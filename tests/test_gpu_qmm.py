@@ -86,19 +86,55 @@ def test_bf16_activations(qtype, M):
     check_tol(y, ref, bnd, TOL_FP32 if M <= 16 else TOL_BF16, "%s bf16 M=%d" % (qtype, M))
 
 
-@pytest.mark.parametrize("qtype", ["Q4_K", "Q6_K"])
-def test_workspace_entry_point(qtype):
+@pytest.mark.parametrize("qtype,N,K,M", [("Q4_K", 9728, 2560, 512), ("Q6_K", 2560, 9728, 600), ("Q4_0", 256, 2560, 64)])
+def test_workspace_entry_point(qtype, N, K, M):
+    """qmm_ws with its scratch (a bf16 copy of x read at the plan's full width, K splits added by a second
+    kernel) and qmm (no scratch: x converted inside the kernel, splits added in a cluster): both within the
+    tolerance of the oracle on sampled outputs, and a call repeated gives the same bits."""
     torch = torch_cuda()
-    N, K, M = 256, 2560, 64
     wq, x = _case(qtype, N, K, M, seed=5)
     nb = qmm.qmm_workspace_size(qtype, N, K, M)
-    assert nb > 0
-    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    assert nb >= M * K * 2
+    ws = torch.empty(max(nb, 1), dtype=torch.uint8, device="cuda") if nb else None
     y = _run(qmm.qmm_ws, wq, qtype, N, K, x, workspace=ws)
+    y1 = _run(qmm.qmm_ws, wq, qtype, N, K, x, workspace=ws)
     y2 = _run(qmm.qmm, wq, qtype, N, K, x)
-    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
+    assert np.array_equal(y.view(np.uint32), y1.view(np.uint32))
+    g = np.random.default_rng(M)
+    ms, ns = g.integers(0, M, 500), g.integers(0, N, 500)
+    ref, bnd = oracle.qmm_sampled(qtype, wq, N, K, x, ms, ns)
+    check_tol(y[ms, ns], ref, bnd, TOL_BF16, qtype + " qmm_ws")
+    check_tol(y2[ms, ns], ref, bnd, TOL_BF16, qtype + " qmm")
+
+
+@pytest.mark.parametrize("qtype", ["Q4_K", "Q6_K", "Q4_0", "Q8_0", "A4G64"])
+@pytest.mark.parametrize("M", [17, 40, 100, 130, 260])
+def test_k_split_in_cluster(qtype, M):
+    """Few row blocks and a long K make the plan split K over a cluster of up to 8 CTAs that add their
+    partials in split order in shared memory: element-wise parity with the oracle, bit-identity across the
+    token tiles, with binary32 (converted in the kernel) and bf16 activations."""
+    N, K = 200, 4096
+    wq, x = _case(qtype, N, K, M, seed=M + 3)
     ref, bnd = oracle.qmm(qtype, wq, N, K, x)
-    check_tol(y, ref, bnd, TOL_BF16, qtype)
+    outs = [_run(qmm.qmm_with_tile, wq, qtype, N, K, x, tile=t) for t in (32, 64, 128)]
+    check_tol(outs[0], ref, bnd, TOL_BF16, "%s M=%d" % (qtype, M))
+    for t, o in zip((64, 128), outs[1:]):
+        assert bit_differences(o, outs[0]) == 0, "%s M=%d: tile %d differs" % (qtype, M, t)
+    y = _run(qmm.qmm, wq, qtype, N, K, x)
+    assert bit_differences(y, outs[0]) == 0
+    # with scratch (M > 32): the partial tiles go through global memory to a second kernel, in split order
+    torch = torch_cuda()
+    nb = qmm.qmm_workspace_size(qtype, N, K, M)
+    assert (nb > 0) == (M > 32)
+    if nb:
+        assert qmm.qmm_plan_info(qtype, N, K, M)[1] > 1
+        ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        yw = _run(qmm.qmm_ws, wq, qtype, N, K, x, workspace=ws)
+        check_tol(yw, ref, bnd, TOL_BF16, "%s qmm_ws M=%d" % (qtype, M))
+    xb = synthetic.activations(M, K, seed=M + 3, bf16=True)
+    yb = _run(qmm.qmm, wq, qtype, N, K, xb)
+    refb, bndb = oracle.qmm(qtype, wq, N, K, xb)
+    check_tol(yb, refb, bndb, TOL_BF16, "%s bf16 M=%d" % (qtype, M))
 
 
 @pytest.mark.parametrize("tile", [0, 32, 64, 128])

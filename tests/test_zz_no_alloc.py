@@ -4,7 +4,8 @@ they run (its scratch lives in one device array the library owns).
 Checked through the C-ABI against qmm() on the same inputs, within the tolerance the parity tests use
 (the tensor-core class, 4e-3 * sum |w x| with the bound from the oracle), on two calls in a row with
 different inputs — the second call runs on whatever the first left in the shared array. Shapes cover the
-tensor-core path with and without the split-K partials, and the mat-vec path that needs no scratch.
+tensor-core path that reads a bf16 copy of x from the array, without and with a K split added inside a
+cluster, and the mat-vec path that needs no scratch.
 This file is collected last so that a failure here stops a run only after every other test has run.
 """
 import numpy as np
@@ -18,8 +19,8 @@ from gpu_util import TOL_BF16, TOL_FP32, check_tol, dev, torch_cuda
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    ("Q4_K", 9728, 2560, 512),   # tensor-core path, bf16 copy of x only
-    ("Q6_K", 1024, 2560, 100),   # tensor-core path with split-K partials
+    ("Q4_K", 9728, 2560, 512),   # tensor-core path, bf16 copy of x in the array
+    ("Q6_K", 1024, 2560, 100),   # tensor-core path, bf16 copy of x; K split over a cluster
     ("Q4_0", 256, 512, 7),       # mat-vec path: no scratch
 ]
 
@@ -30,6 +31,8 @@ def test_noalloc_matches_qmm_twice(qtype, N, K, M):
     qmm.build()
     need = qmm.qmm_workspace_size(qtype, N, K, M)
     assert need <= qmm.NOALLOC_SCRATCH_BYTES
+    if M > 32:
+        assert need >= M * K * 2          # these cases use the array
     wq_h = oracle.quantize(qtype, synthetic.weights(N, K, seed=N + M))
     wq = dev(wq_h)
     tol = TOL_FP32 if M <= 16 else TOL_BF16
@@ -48,8 +51,6 @@ def test_noalloc_matches_qmm_twice(qtype, N, K, M):
         _, bnd = oracle.qmm_sampled(qtype, wq_h, N, K, x_h, ms, ns)
         check_tol(a[ms, ns], b[ms, ns].astype(np.float64), bnd, tol, "noalloc vs qmm, call %d" % call)
         assert np.all(np.isfinite(a))
-        # the same kernels run, so the results agree exactly as well
-        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
 
 
 def test_noalloc_refuses_oversized_scratch():

@@ -12,7 +12,7 @@ import ctypes
 import os
 
 __all__ = ["QmmError", "TYPES", "TYPE_ID", "X_BF16", "X_PER_SLOT", "build", "lib", "qmm", "qmm_ws", "qmm_workspace_size",
-           "qmm_launch_count", "qmm_noalloc", "NOALLOC_SCRATCH_BYTES",
+           "qmm_launch_count", "qmm_plan_info", "qmm_noalloc", "NOALLOC_SCRATCH_BYTES",
            "qmm_id", "qmm_with_tile", "qmm_pick_tile", "qmm_pick_path", "qmm_dequant", "qmm_quantize",
            "qmm_type_info", "qmm_get_status", "qmm_debug_stall", "qmm_strerror", "row_bytes", "EXPORTS"]
 
@@ -28,7 +28,7 @@ STATUS_BAD_ID, STATUS_TIMEOUT = 0x1, 0x2
 
 # Every symbol include/qmm.h declares.
 EXPORTS = ["qmm", "qmm_ws", "qmm_workspace_size", "qmm_noalloc", "qmm_id", "qmm_with_tile", "qmm_pick_tile",
-           "qmm_pick_path", "qmm_launch_count", "qmm_dequant", "qmm_quantize", "qmm_type_info", "qmm_get_status",
+           "qmm_pick_path", "qmm_launch_count", "qmm_plan_info", "qmm_dequant", "qmm_quantize", "qmm_type_info", "qmm_get_status",
            "qmm_debug_stall", "qmm_strerror"]
 NOALLOC_SCRATCH_BYTES = 64 << 20   # QMM_NOALLOC_SCRATCH_BYTES
 
@@ -65,6 +65,7 @@ def lib():
             "qmm_pick_tile": ([I64], I),
             "qmm_pick_path": ([I, I64, I64, I64], I),
             "qmm_launch_count": ([I, I64, I64, I64], I),
+            "qmm_plan_info": ([I, I64, I64, I64, ctypes.POINTER(I), ctypes.POINTER(I)], I),
             "qmm_dequant": ([P, I, I64, I64, P, P], I),
             "qmm_quantize": ([P, I, I64, I64, P, P], I),
             "qmm_type_info": ([I, ctypes.POINTER(I), ctypes.POINTER(I)], I),
@@ -134,6 +135,16 @@ def qmm_pick_path(qtype, N: int, K: int, M: int) -> int:
 
 def qmm_launch_count(qtype, N: int, K: int, M: int, x_bf16: bool = False) -> int:
     return lib().qmm_launch_count(_qt(qtype) | (X_BF16 if x_bf16 else 0), int(N), int(K), int(M))
+
+
+def qmm_plan_info(qtype, N: int, K: int, M: int, x_bf16: bool = False):
+    """(path, K split, token columns per CTA) of the work plan (0, 0, 0 on the mat-vec path)."""
+    S, c = ctypes.c_int(), ctypes.c_int()
+    rc = lib().qmm_plan_info(_qt(qtype) | (X_BF16 if x_bf16 else 0), int(N), int(K), int(M), ctypes.byref(S),
+                             ctypes.byref(c))
+    if rc < 0:
+        raise QmmError(rc, "qmm_plan_info")
+    return rc, S.value, c.value
 
 
 def qmm_workspace_size(qtype, N: int, K: int, M: int, x_bf16: bool = False) -> int:

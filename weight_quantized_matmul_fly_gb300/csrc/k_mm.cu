@@ -8,7 +8,9 @@
 //     MMA's N), J*T <= 256, or 512 for large M (the whole tensor memory); the J tiles share every decoded
 //     slab, so a larger J*T divides the decoding work per multiply-add (J = 1..6 or 8, only as many tiles
 //     as the tokens need);
-//   - warp 0 loads the J*T x 64 bf16 activation tile of each K step by TMA (rows past M read as zero);
+//   - warp 0 loads the J*T x 64 activation tile of each K step by TMA (rows past M read as zero): bf16
+//     straight into the operand stage, or binary32 into a staging slot from which the decoder group of
+//     that step rounds it to bf16 into the operand stage (no separate conversion pass);
 //   - warps 2..17 decode the 128 x 64 weight slab of each step to bf16 (round to nearest even of the
 //     binary32 value) straight into the 128-byte-swizzled K-major layout tcgen05 reads; they form two
 //     groups of 8 that take alternate K steps, so each keeps the raw bytes of its next two steps (four K
@@ -16,8 +18,9 @@
 //   - warp 1 issues, per step, 4 (K = 16) tcgen05.mma of N = min(J*T, 256) tokens (two at 512) into TMEM
 //     and commits them to the stage's "empty" barrier, which hands the stage back to the producer and the
 //     decoders;
-//   - the decoder warps then read TMEM with tcgen05.ld and write y (or, when K is split over CTAs, a
-//     binary32 partial that a second kernel adds up in a fixed order).
+//   - the decoder warps then read TMEM with tcgen05.ld and write y; when K is split over S CTAs they form
+//     a thread block cluster and add their partial tiles in split order through distributed shared
+//     memory, so a call is one kernel and needs no scratch.
 // Bit-identity across T: every output element sees the same K steps, the same K=16 MMAs in the same
 // order and the same K split whatever T is (candle PR 4056, section "Same results, bit for bit").
 #include <cuda.h>
@@ -32,19 +35,33 @@ namespace mm {
 
 constexpr int BM = 128;            // weight rows per CTA
 constexpr int BK = 64;             // columns per K step: one 128-byte swizzle row of bf16
-constexpr int MAX_STAGES = 4;
+constexpr int MAX_STAGES = 8;
+constexpr int PF = 2;              // K steps of its own group a decoder warp keeps in flight (raw bytes in registers)
 constexpr int A_STAGE = BM * BK * 2;   // 16 KB
 constexpr int NDEC = 16;               // decoder / epilogue warps: two groups of 8 taking alternate K steps
 constexpr int NGRP = NDEC / 8;         // decoder groups (one slab = 8 warps x 16 rows)
 constexpr int THREADS = 32 * (2 + NDEC);
 
+constexpr int MAX_XSLOTS = 6;
+constexpr int MAX_SPLIT = 8;       // K splits of one output tile: CTAs of one (portable-size) cluster
+
 __host__ __device__ constexpr int b_stage_bytes(int TN) { return TN * BK * 2; }
-// Operand stages: four up to 256 tokens per CTA; two at 512 (80 KB each). At 512 tokens one K step of MMAs
-// takes about twice as long as decoding the step's weights, so two stages keep the tensor core fed.
-__host__ __device__ constexpr int stages_of(int TN) { return TN > 256 ? 2 : 4; }
-__host__ __device__ constexpr int smem_bytes(int TN) {
-    return 1024 /* alignment slack */ + stages_of(TN) * (A_STAGE + b_stage_bytes(TN)) + 256 /* barriers */;
+__host__ __device__ constexpr int x_slot_bytes(int TN) { return TN * BK * 4; }   // binary32 staging of a K step
+// Operand stages: four up to 256 token columns per CTA, two at 512 (80 KB each; there one K step of MMAs
+// takes about as long as decoding the step's weights). More stages measured no faster, and the shared memory
+// they take comes out of the L1 cache the decoders' weight loads go through. With binary32 activations
+// converted in the kernel, staging slots for them take part of the room.
+__host__ __device__ constexpr int stages_of(int TN, bool xf32) {
+    return xf32 ? (TN > 96 ? 3 : (TN > 32 ? 4 : 8)) : (TN > 256 ? 2 : 4);
 }
+__host__ __device__ constexpr int xslots_of(int TN, bool xf32) { return xf32 ? (TN > 64 ? 3 : (TN > 32 ? 6 : 4)) : 0; }
+__host__ __device__ constexpr int smem_bytes(int TN, bool xf32) {
+    return 1024 /* alignment slack */ + stages_of(TN, xf32) * (A_STAGE + b_stage_bytes(TN)) +
+           xslots_of(TN, xf32) * x_slot_bytes(TN) + 256 /* barriers */;
+}
+
+// Epilogue: which of the NDEC/4 column parts decoder warp `warp` drains (its lane quarter is warp & 3).
+__device__ __forceinline__ int part_of(int warp) { return (warp - 2) >> 2; }
 
 // Byte offset of the 16-byte piece p (bf16 columns 8p .. 8p+7) of row r in a 128-byte-swizzled tile.
 __device__ __forceinline__ uint32_t sw128_off(int r, int p) {
@@ -194,44 +211,66 @@ template <> struct Slab<T_Q4_0> {
 
 struct Smem {
     uint64_t full_b[MAX_STAGES], full_a[MAX_STAGES], empty[MAX_STAGES], done;
+    uint64_t xfull[MAX_XSLOTS], xempty[MAX_XSLOTS];
     uint32_t tmem;
     int abort;
 };
 
-// out = y (S == 1) or the partial buffer of this K split (S > 1), both M x N binary32 row-major.
-template <int QT, int T, int J>
+// y = x * dequant(W)^T for a 128-row block, TN = T*J token columns and one K split of the work plan.
+//   XF32 = false: x is bfloat16 (the caller's, or the bf16 copy of binary32 activations); warp 0 loads the
+//                 activation tile of each K step straight into the operand stage by TMA (128-byte swizzle).
+//   XF32 = true:  x is binary32; warp 0 loads its tile by TMA into a ring of staging slots, and the decoder
+//                 group that decodes the K step's weights also rounds the step's activations to bfloat16
+//                 (nearest even) into the operand stage, so no separate conversion pass is needed.
+// When K is split over S CTAs (gridDim.z = S > 1), the partial tiles are added in split order in one of two
+// ways, with the same result bit for bit:
+//   part == nullptr: the S CTAs of an output tile form a thread block cluster; each stores its binary32
+//     partial tile into its own shared memory and, after a cluster barrier, rank r adds the S partials of
+//     its share of the tile's columns in rank (= split) order and writes y: no scratch, no second kernel;
+//   part != nullptr: each CTA writes its partial tile to part + split * split_stride (M x N binary32), and a
+//     second kernel adds them in split order. Measured faster when the kernel follows the separate bf16
+//     conversion pass of x (a cluster launch starts later behind a kernel that is not one).
+template <int QT, int T, int J, bool XF32>
 __global__ void __launch_bounds__(THREADS, 1)
     mm_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint8_t *__restrict__ wq, int N, int64_t K,
-              int64_t rowbytes, int M, float *__restrict__ out, int64_t split_stride, int ksteps_per_split,
-              unsigned int *status) {
+              int64_t rowbytes, int M, float *__restrict__ y, int ksteps_per_split, float *__restrict__ part,
+              int64_t split_stride, unsigned int *status) {
     constexpr int TN = T * J;
-    constexpr int STAGES = stages_of(TN);
+    constexpr int STAGES = stages_of(TN, XF32);
+    constexpr int XSLOTS = xslots_of(TN, XF32);
     constexpr uint32_t TMEM_COLS = TN <= 32 ? 32 : (TN <= 64 ? 64 : (TN <= 128 ? 128 : (TN <= 256 ? 256 : 512)));
     // One MMA covers up to 256 token columns (all J tiles of T at once; the tiles are contiguous in
     // shared memory and in TMEM): N = MN per instruction, NMMA instructions per K = 16.
     constexpr int MN = TN > 256 ? 256 : TN, NMMA = TN / MN;
     static_assert(MN % 16 == 0 && TN % MN == 0, "MMA N");
+    static_assert(!XF32 || TN <= 128, "binary32 activations are converted in-kernel up to 128 token columns");
+    static_assert(smem_bytes(TN, XF32) <= 227 * 1024, "shared memory of one CTA");
     constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, MN);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *sA = smem;
     uint8_t *sB = smem + STAGES * A_STAGE;
-    Smem *sm = reinterpret_cast<Smem *>(sB + STAGES * b_stage_bytes(TN));
+    uint8_t *sX = sB + STAGES * b_stage_bytes(TN);              // binary32 staging slots (XF32)
+    Smem *sm = reinterpret_cast<Smem *>(sX + XSLOTS * x_slot_bytes(TN));
+    float *red = reinterpret_cast<float *>(smem);              // after the main loop: this CTA's partial tile
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n0 = blockIdx.x * BM, m0 = blockIdx.y * TN;
-    const int split = blockIdx.z;
+    const int S = (int)gridDim.z, split = blockIdx.z;
     const int ktotal = (int)((K + BK - 1) / BK);
     const int kbeg = split * ksteps_per_split;
     const int kend = (kbeg + ksteps_per_split < ktotal) ? kbeg + ksteps_per_split : ktotal;
     const int nsteps = kend > kbeg ? kend - kbeg : 0;
-    float *y = out + (int64_t)split * split_stride;
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(&sm->full_b[s], 1);
             ptx::mbar_init(&sm->full_a[s], 8);   // the 8 warps of the group that decodes this step
             ptx::mbar_init(&sm->empty[s], 1);
+        }
+        for (int j = 0; j < XSLOTS; ++j) {
+            ptx::mbar_init(&sm->xfull[j], 1);
+            ptx::mbar_init(&sm->xempty[j], 8);   // the 8 warps of the group that converted the slot
         }
         ptx::mbar_init(&sm->done, 1);
         sm->abort = 0;
@@ -255,25 +294,32 @@ __global__ void __launch_bounds__(THREADS, 1)
         // decoded meanwhile)
         asm volatile("griddepcontrol.wait;" ::: "memory");
         if (lane == 0) {
+            constexpr int NB = XF32 ? XSLOTS : STAGES;     // ring the loads go to
             int issued = 0;
             for (int i = 0; i < nsteps; ++i) {
-                const int s = i % STAGES;
-                if (i >= STAGES && !ptx::mbar_wait(&sm->empty[s], ((i / STAGES) - 1) & 1, status)) {
+                const int s = i % NB;
+                uint64_t *freed = XF32 ? &sm->xempty[s] : &sm->empty[s];
+                if (i >= NB && !ptx::mbar_wait(freed, ((i / NB) - 1) & 1, status)) {
                     sm->abort = 1;
                     break;
                 }
                 if (*(volatile int *)&sm->abort) break;
-                ptx::mbar_arrive_expect_tx(&sm->full_b[s], (uint32_t)b_stage_bytes(TN));
-                // a tensor-map box has at most 256 rows: 512 tokens take two boxes
+                if constexpr (XF32) {
+                    ptx::mbar_arrive_expect_tx(&sm->xfull[s], (uint32_t)x_slot_bytes(TN));
+                    ptx::tma_load_2d(sX + s * x_slot_bytes(TN), &tmap_x, (kbeg + i) * BK, m0, &sm->xfull[s]);
+                } else {
+                    ptx::mbar_arrive_expect_tx(&sm->full_b[s], (uint32_t)b_stage_bytes(TN));
+                    // a tensor-map box has at most 256 rows: 512 tokens take two boxes
 #pragma unroll
-                for (int q = 0; q < (TN > 256 ? TN / 256 : 1); ++q)
-                    ptx::tma_load_2d(sB + s * b_stage_bytes(TN) + q * 256 * 128, &tmap_x, (kbeg + i) * BK,
-                                     m0 + 256 * q, &sm->full_b[s]);
+                    for (int q = 0; q < (TN > 256 ? TN / 256 : 1); ++q)
+                        ptx::tma_load_2d(sB + s * b_stage_bytes(TN) + q * 256 * 128, &tmap_x, (kbeg + i) * BK,
+                                         m0 + 256 * q, &sm->full_b[s]);
+                }
                 issued = i + 1;
             }
-            // every requested tile lands before the CTA may exit
-            for (int i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
-                ptx::mbar_wait(&sm->full_b[i % STAGES], (i / STAGES) & 1, status);
+            // every requested tile lands before the CTA may go on (its shared memory is reused below)
+            for (int i = (issued > NB ? issued - NB : 0); i < issued; ++i)
+                ptx::mbar_wait(XF32 ? &sm->xfull[i % NB] : &sm->full_b[i % NB], (i / NB) & 1, status);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer
@@ -282,7 +328,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int i = 0; i < nsteps; ++i) {
                 const int s = i % STAGES;
                 const uint32_t par = (i / STAGES) & 1;
-                if (!ptx::mbar_wait(&sm->full_a[s], par, status) || !ptx::mbar_wait(&sm->full_b[s], par, status)) {
+                if (!ptx::mbar_wait(&sm->full_a[s], par, status) ||
+                    (!XF32 && !ptx::mbar_wait(&sm->full_b[s], par, status))) {
                     sm->abort = 1;
                     break;
                 }
@@ -311,20 +358,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         const bool row_ok = row < N;
         const uint8_t *wrow = wq + (int64_t)(row_ok ? row : N - 1) * rowbytes;
         const int nchunks = (int)((K + 31) / 32);
-        const uint32_t sA_u32 = ptx::smem_u32(sA);
+        const uint32_t sA_u32 = ptx::smem_u32(sA), sB_u32 = ptx::smem_u32(sB);
         using SL = Slab<QT>;
-        // raw bytes of the group's next two K steps are in flight while a step is decoded
-        typename SL::Raw r0, r1, r2;
+        // raw bytes of the group's next PF K steps are in flight while a step is decoded (rw[0] is the
+        // step being decoded, rw[PF] the one requested during it)
+        typename SL::Raw rw[PF + 1];
         if constexpr (SL::FAST) {
             const int c0 = 2 * (kbeg + grp) + h;
-            if (grp < nsteps && c0 < nchunks) SL::load(r0, wrow, c0);
-            if (grp + NGRP < nsteps && c0 + 2 * NGRP < nchunks) SL::load(r1, wrow, c0 + 2 * NGRP);
+#pragma unroll
+            for (int j = 0; j < PF; ++j)
+                if (grp + j * NGRP < nsteps && c0 + 2 * j * NGRP < nchunks) SL::load(rw[j], wrow, c0 + 2 * j * NGRP);
         }
         for (int i = grp; i < nsteps; i += NGRP) {
             const int s = i % STAGES;
             const int c = 2 * (kbeg + i) + h;
             if constexpr (SL::FAST) {
-                if (i + 2 * NGRP < nsteps && c + 4 * NGRP < nchunks) SL::load(r2, wrow, c + 4 * NGRP);
+                if (i + PF * NGRP < nsteps && c + 2 * PF * NGRP < nchunks) SL::load(rw[PF], wrow, c + 2 * PF * NGRP);
             }
             if (i >= STAGES && !ptx::mbar_wait(&sm->empty[s], ((i / STAGES) - 1) & 1, status)) {
                 sm->abort = 1;
@@ -334,7 +383,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t o[16];
             if (row_ok && c < nchunks) {
                 if constexpr (SL::FAST) {
-                    SL::decode(r0, c, o);
+                    SL::decode(rw[0], c, o);
                 } else {
                     float w[32];
                     decode_chunk<QT>(wrow, c, K, w);
@@ -350,46 +399,137 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int p = 0; p < 4; ++p)
                 ptx::st_shared_v4(a_base + sw128_off(r_local, 4 * h + p), o[4 * p], o[4 * p + 1], o[4 * p + 2],
                                   o[4 * p + 3]);
+            if constexpr (XF32) {
+                // this step's activations: binary32 staging slot -> bf16 operand stage, 8 columns (one 16-byte
+                // piece of the swizzled row) per thread and pass; rows past M were read as zero by the TMA
+                const int xs = i % XSLOTS;
+                if (!ptx::mbar_wait(&sm->xfull[xs], (i / XSLOTS) & 1, status)) {
+                    sm->abort = 1;
+                    break;
+                }
+                const float *xsrc = reinterpret_cast<const float *>(sX + xs * x_slot_bytes(TN));
+                const uint32_t b_base = sB_u32 + s * b_stage_bytes(TN);
+                const int gt = 32 * dw + lane;              // thread index within the group
+#pragma unroll
+                for (int pc = gt; pc < TN * 8; pc += 256) {
+                    const int rr = pc >> 3, pp = pc & 7;
+                    const float4 a = *reinterpret_cast<const float4 *>(xsrc + rr * BK + 8 * pp);
+                    const float4 b = *reinterpret_cast<const float4 *>(xsrc + rr * BK + 8 * pp + 4);
+                    ptx::st_shared_v4(b_base + sw128_off(rr, pp), pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w),
+                                      pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&sm->xempty[xs]);
+            }
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&sm->full_a[s]);
             if constexpr (SL::FAST) {
-                r0 = r1;
-                r1 = r2;
+#pragma unroll
+                for (int j = 0; j < PF; ++j) rw[j] = rw[j + 1];
             }
         }
-        // ---------------- epilogue: TMEM lanes = weight rows, columns = tokens (written only once the
-        // preceding kernel has completed)
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-        constexpr int PARTS = NDEC / 4;         // warps per TMEM lane quarter; they split the columns
-        const int q = warp & 3;                 // TMEM lane quarter this warp may access
-        const int part = (warp - 2) >> 2;       // (q, part) runs over all quarters x parts once
-        const int r = n0 + 32 * q + lane;
-        if (nsteps > 0) {
-            const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(&sm->done, 0, status) && !*(volatile int *)&sm->abort);
-            ptx::tc_fence_after();
-            if (ok) {
-                const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
-                for (int c0 = 16 * part; c0 < TN; c0 += 16 * PARTS) {
-                    uint32_t v[16];
+    }
+
+    // ---------------- epilogue: TMEM lanes = weight rows, columns = tokens. Every MMA has completed once
+    // `done` has; the operand stages are then free (the producer waited for all its loads above).
+    constexpr int PARTS = NDEC / 4;             // warps per TMEM lane quarter; they split the columns
+    const bool dec = warp >= 2;
+    const int q = warp & 3;                     // TMEM lane quarter this warp may access
+    const int pw = part_of(warp);               // (q, pw) runs over all quarters x parts once
+    const int r = 32 * q + lane;                // row within the block
+    // y (and the scratch partials) are written only once the preceding kernel has completed; with the split
+    // added inside the cluster every thread writes y
+    if (dec || (S > 1 && !part)) asm volatile("griddepcontrol.wait;" ::: "memory");
+    bool ok = true;
+    if (dec && nsteps > 0) {
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(&sm->done, 0, status) && !*(volatile int *)&sm->abort);
+        ptx::tc_fence_after();
+    }
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
+    if (S == 1) {
+        if (dec && ok) {
+            for (int c0 = 16 * pw; c0 < TN; c0 += 16 * PARTS) {
+                uint32_t v[16];
+                if (nsteps > 0) {
                     ptx::tmem_ld_32x32b_x16(lane_base + c0, v);
                     ptx::tmem_ld_wait();
-                    if (r < N) {
+                } else {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int tok = m0 + c0 + j;
-                            if (tok < M) y[(int64_t)tok * N + r] = __uint_as_float(v[j]);
-                        }
+                    for (int j = 0; j < 16; ++j) v[j] = 0u;       // an empty K range contributes zeros
+                }
+                if (n0 + r < N) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int tok = m0 + c0 + j;
+                        if (tok < M) y[(int64_t)tok * N + n0 + r] = __uint_as_float(v[j]);
                     }
                 }
             }
-        } else {
-            // an empty K split contributes zeros
-            for (int c0 = 16 * part; c0 < TN; c0 += 16 * PARTS)
-                for (int j = 0; j < 16; ++j) {
-                    const int tok = m0 + c0 + j;
-                    if (r < N && tok < M) y[(int64_t)tok * N + r] = 0.0f;
+        }
+    } else if (part) {
+        float *py = part + (int64_t)split * split_stride;
+        if (dec) {
+            for (int c0 = 16 * pw; c0 < TN; c0 += 16 * PARTS) {
+                uint32_t v[16];
+                if (nsteps > 0 && ok) {
+                    ptx::tmem_ld_32x32b_x16(lane_base + c0, v);
+                    ptx::tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] = 0u;
                 }
+                if (n0 + r < N) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int tok = m0 + c0 + j;
+                        if (tok < M) py[(int64_t)tok * N + n0 + r] = __uint_as_float(v[j]);
+                    }
+                }
+            }
+        }
+    } else {
+        // every load the producer issued has landed before the operand stages are reused
+        __syncthreads();
+        // K split over the cluster: rounds of RC columns. Each CTA stores its partial [RC columns][128 rows]
+        // into its own (now idle) operand stages; after a cluster barrier, rank `split` adds up, for columns
+        // [split*cw, split*cw + cw) of the round, the S partials in rank order and writes y; a second barrier
+        // keeps every CTA's shared memory alive until all ranks have read it.
+        constexpr int RC = TN > 256 ? 256 : TN;
+        const int cw = (RC + S - 1) / S;
+        for (int rc0 = 0; rc0 < TN; rc0 += RC) {
+            if (dec) {
+                for (int c0 = 16 * pw; c0 < RC; c0 += 16 * PARTS) {
+                    uint32_t v[16];
+                    if (nsteps > 0 && ok) {
+                        ptx::tmem_ld_32x32b_x16(lane_base + rc0 + c0, v);
+                        ptx::tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v[j] = 0u;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) red[(c0 + j) * BM + r] = __uint_as_float(v[j]);
+                }
+            }
+            ptx::cluster_sync();
+            const int cb = split * cw, ce = cb + cw < RC ? cb + cw : RC;
+            for (int e = tid + cb * BM; e < ce * BM; e += THREADS) {
+                const int col = e / BM, row = e - col * BM;
+                const int tok = m0 + rc0 + col;
+                if (tok >= M || n0 + row >= N) continue;
+                // the S loads are issued back to back, then added in rank order
+                float v[MAX_SPLIT];
+#pragma unroll
+                for (int qq = 0; qq < MAX_SPLIT; ++qq)
+                    if (qq < S) v[qq] = ptx::ld_dsmem_f32(ptx::mapa(red + e, (uint32_t)qq));
+                float a = v[0];
+#pragma unroll
+                for (int qq = 1; qq < MAX_SPLIT; ++qq)
+                    if (qq < S) a += v[qq];
+                y[(int64_t)tok * N + n0 + row] = a;
+            }
+            ptx::cluster_sync();
         }
     }
     ptx::tc_fence_before();
@@ -406,7 +546,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
-// y[i] = sum over s of part[s][i], s ascending (deterministic K-split reduction).
+// y[i] = sum over s of part[s][i], s ascending (the K splits' partial tiles added in split order).
 __global__ void splitk_reduce_kernel(const float4 *__restrict__ part, int64_t stride4, int S, float4 *__restrict__ y,
                                      int64_t n4) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -461,40 +601,53 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
     return fn;
 }
 
-static bool make_x_tmap(CUtensorMap *map, const void *xb, int64_t M, int64_t K, int rows) {
+// Tensor map of the activations: bf16 rows read as 128-byte-swizzled K-major tiles straight into an operand
+// stage, or binary32 rows read unswizzled into a staging slot (64 columns = 256 bytes per row). Rows past M
+// and columns past K read as zero.
+static bool make_x_tmap(CUtensorMap *map, const void *x, bool f32, int64_t M, int64_t K, int rows) {
     auto enc = encode_tiled();
     if (!enc) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * (f32 ? 4 : 2)};
     const cuuint32_t box[2] = {(cuuint32_t)mm::BK, (cuuint32_t)rows};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(xb), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    CUresult r = enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                     const_cast<void *>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     f32 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
 struct MmPlan {
-    int S;      // K split
+    int S;      // K split (CTAs of one cluster)
     int cols;   // token columns per CTA
 };
 
 namespace {
 
-// Launch with programmatic stream serialization: the kernel may start while its predecessor in the stream
-// finishes; it orders its own memory accesses with griddepcontrol.wait. Returns 0 or -6.
+// Launch with programmatic stream serialization (the kernel may start while its predecessor in the stream
+// finishes; it orders its own memory accesses with griddepcontrol.wait) and, for S > 1, clusters of the S
+// CTAs that split one output tile's K range. Returns 0 or -6.
 template <typename... Args>
-int launch_pdl(const void *kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+int launch_pdl(const void *kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, int cluster_z, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    int na = 1;
+    if (cluster_z > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 1;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = (unsigned)cluster_z;
+        na = 2;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = na;
     void *argv[] = {reinterpret_cast<void *>(&args)...};
     return cudaLaunchKernelExC(&cfg, kern, argv) == cudaSuccess ? 0 : -6;
 }
@@ -513,43 +666,63 @@ inline int tiles_per_cta(int T, int64_t M, int cols) {
     return j;
 }
 
-template <int QT, int T, int J>
-int launch_mm_t(const void *wq, int64_t N, int64_t K, const void *xb, int64_t M, float *out, int S, int kps,
-                int64_t split_stride, unsigned int *status, cudaStream_t st) {
-    CUtensorMap map;
-    if (!make_x_tmap(&map, xb, M, K, T * J > 256 ? 256 : T * J)) return -6;
-    auto kern = mm::mm_kernel<QT, T, J>;
-    const int smem = mm::smem_bytes(T * J);
-    static bool attr_set[kMaxDevices] = {};   // once per kernel instance and device
+// Sets the kernel's shared-memory attribute once per device. Returns false on failure.
+template <int QT, int T, int J, bool XF32>
+bool mm_attrs() {
+    static bool attr_set[kMaxDevices] = {};
     const int devi = current_device_index();
     if (!attr_set[devi]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -6;
+        auto kern = mm::mm_kernel<QT, T, J, XF32>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, mm::smem_bytes(T * J, XF32)) !=
+            cudaSuccess)
+            return false;
         attr_set[devi] = true;
     }
-    dim3 grid((unsigned)((N + mm::BM - 1) / mm::BM), (unsigned)((M + T * J - 1) / (T * J)), (unsigned)S);
+    return true;
+}
+
+template <int QT, int T, int J, bool XF32>
+int launch_mm_t(const void *wq, int64_t N, int64_t K, const void *x, int64_t M, float *y, int S, int kps, float *part,
+                int64_t split_stride, unsigned int *status, cudaStream_t st) {
+    constexpr int TN = T * J;
+    CUtensorMap map;
+    if (!make_x_tmap(&map, x, XF32, M, K, TN > 256 ? 256 : TN)) return -6;
+    if (!mm_attrs<QT, T, J, XF32>()) return -6;
+    auto kern = mm::mm_kernel<QT, T, J, XF32>;
+    dim3 grid((unsigned)((N + mm::BM - 1) / mm::BM), (unsigned)((M + TN - 1) / TN), (unsigned)S);
     const int64_t rb = row_bytes(QT, K);
     const uint8_t *w8 = static_cast<const uint8_t *>(wq);
     const int Ni = (int)N, Mi = (int)M;
-    return launch_pdl(reinterpret_cast<const void *>(kern), grid, dim3(mm::THREADS), (size_t)smem, st, map, w8, Ni, K,
-                      rb, Mi, out, split_stride, kps, status);
+    return launch_pdl(reinterpret_cast<const void *>(kern), grid, dim3(mm::THREADS),
+                      (size_t)mm::smem_bytes(TN, XF32), st, part ? 1 : S, map, w8, Ni, K, rb, Mi, y, kps, part,
+                      split_stride, status);
 }
 
 struct MmLaunch {
     int tile, J;
+    bool xf32;
     const void *wq;
     int64_t N, K;
-    const void *xb;
+    const void *x;
     int64_t M;
-    float *out;
+    float *y;
     int S, kps;
+    float *part;
     int64_t split_stride;
     unsigned int *status;
     cudaStream_t st;
     template <int QT, int T, int JJ> int go_j() {
-        if constexpr ((T * JJ <= 256 && ((JJ & (JJ - 1)) == 0 || T == 32 || (T == 64 && JJ == 3))) ||
-                      (T >= 64 && T * JJ <= 512 && (JJ & (JJ - 1)) == 0))
-            return launch_mm_t<QT, T, JJ>(wq, N, K, xb, M, out, S, kps, split_stride, status, st);
-        else return -7;
+        constexpr int TN = T * JJ;
+        constexpr bool shape_ok = (TN <= 256 && ((JJ & (JJ - 1)) == 0 || T == 32 || (T == 64 && JJ == 3))) ||
+                                  (T >= 64 && TN <= 512 && (JJ & (JJ - 1)) == 0);
+        if constexpr (!shape_ok) {
+            return -7;
+        } else {
+            if (!xf32) return launch_mm_t<QT, T, JJ, false>(wq, N, K, x, M, y, S, kps, part, split_stride, status, st);
+            if constexpr (TN <= 128)
+                return launch_mm_t<QT, T, JJ, true>(wq, N, K, x, M, y, S, kps, part, split_stride, status, st);
+            return -7;
+        }
     }
     template <int QT, int T> int go() {
         switch (J) {
@@ -573,22 +746,57 @@ struct MmLaunch {
     }
 };
 
+// CTAs of the tensor-core kernel resident at once when launched in clusters of S (every instance runs one
+// CTA per SM; a cluster must fit in one GPC, which can strand SMs), queried once per device and S.
+int64_t mm_capacity(int S) {
+    static int64_t cache[kMaxDevices][mm::MAX_SPLIT + 1] = {};
+    const int dev = current_device_index();
+    if (S < 1 || S > mm::MAX_SPLIT) return 0;
+    if (cache[dev][S]) return cache[dev][S];
+    int64_t cap = device_sm_count();
+    if (S > 1) {
+        auto kern = mm::mm_kernel<T_Q4_0, 32, 4, false>;
+        int nclusters = 0;
+        if (mm_attrs<T_Q4_0, 32, 4, false>()) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(1, 1, (unsigned)S);
+            cfg.blockDim = dim3(mm::THREADS);
+            cfg.dynamicSmemBytes = (size_t)mm::smem_bytes(128, false);
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 1;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = (unsigned)S;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) != cudaSuccess) nclusters = 0;
+        }
+        // unknown (no device): assume a cluster packs as well as single CTAs
+        cap = nclusters > 0 ? (int64_t)nclusters * S : (device_sm_count() / S) * S;
+    }
+    cache[dev][S] = cap;
+    return cap;
+}
+
 }  // namespace
 
 // Work plan of the tensor-core path: the K split S and the token columns per CTA (128, 256 or 512), a
-// function of (type, N, K, M) only, never of the token tile, so that every tile variant adds the same
-// partial sums in the same order. CTAs of 128 rows run one per SM; the plan minimises the modelled time
-//     waves * (t_wave + ksteps_per_split * t_step(cols, type))  +  (2 S M N * 4 bytes) / HBM bandwidth,
-// where a wave is ceil(CTAs / SMs) and the last term is the partial sums written and read back when K is
-// split. The constants were fitted (about 7 % rms) to a sweep of every split S <= 12 and 128/256/512
-// columns over the seven Qwen3-Embedding-4B projections at 128, 512 and 2048 tokens on GB300: a K step
-// (64 weights) of a CTA costs 0.45 / 0.49 / 0.71 us at 128 / 256 / 512 columns for 4-bit K-quants (the
-// weight decoding, not the tensor core, sets the pace below 512 columns), 1.7 times that for Q6_K, and a
-// wave about 1.4 us to start and drain. Splits keep at least 4 K steps each and leave no split empty.
-MmPlan mm_plan(int qt, int64_t N, int64_t K, int64_t M) {
+// function of (type, N, K, M) and of how a split is added (inside a cluster or by a second kernel) only,
+// never of the token tile, so that every tile variant adds the same partial sums in the same order. CTAs of
+// 128 rows run one per SM. With `cluster` the S CTAs of a split form a cluster (S <= 8), and a wave holds as
+// many of them as the clusters that fit at once; otherwise S <= 32 and a wave is one CTA per SM. The plan
+// minimises the modelled time
+//     waves * (t_wave + ksteps_per_split * t_step(cols, type))  +  2 S M N * 4 bytes / 6 TB/s  (S > 1)
+// A K step (64 weights) of a CTA costs 0.45 / 0.49 / 0.71 us at 128 / 256 / 512 columns for 4-bit K-quants
+// (fitted to a GB300 sweep of every split and column count over the seven Qwen3-Embedding-4B projections at
+// 128, 512 and 2048 tokens; the weight decoding, not the tensor core, sets the pace below 512 columns), 1.7
+// times that for Q6_K; a wave costs about 1.4 us to start and drain; the last term charges the partial
+// tiles (moved through shared memory and read across the cluster), which measured as costly as writing
+// and reading them through HBM: without it, plans with several splits at 512 columns ran 1.2-1.6 times
+// slower than the unsplit ones. Splits keep at least 4 K steps each and leave no split empty.
+MmPlan mm_plan(int qt, int64_t N, int64_t K, int64_t M, bool cluster) {
     const int64_t ksteps = (K + mm::BK - 1) / mm::BK;
     const int64_t rowblocks = (N + mm::BM - 1) / mm::BM;
-    const int64_t nsm = device_sm_count();
     const double t_wave = 1.4, hbm_bytes_per_us = 6.0e6;
     const double type_factor = qt == T_Q6_K ? 1.7 : 1.0;
     MmPlan best{1, 128};
@@ -597,10 +805,12 @@ MmPlan mm_plan(int qt, int64_t N, int64_t K, int64_t M) {
         if (cols > 128 && cols / 2 >= M) break;      // more columns than the tokens need
         const double t_step = type_factor * (cols == 128 ? 0.45 : (cols == 256 ? 0.49 : 0.71));
         const int64_t ctas1 = rowblocks * ((M + cols - 1) / cols);
-        for (int S = 1; S <= 32; ++S) {
+        for (int S = 1; S <= (cluster ? mm::MAX_SPLIT : 32); ++S) {
             const int64_t kps = (ksteps + S - 1) / S;
             if (S > 1 && (ksteps / S < 4 || (S - 1) * kps >= ksteps)) continue;
-            const int64_t waves = (ctas1 * S + nsm - 1) / nsm;
+            const int64_t cap = cluster ? mm_capacity(S) : device_sm_count();
+            if (cap <= 0) continue;
+            const int64_t waves = (ctas1 * S + cap - 1) / cap;
             double t = (double)waves * (t_wave + (double)kps * t_step);
             if (S > 1) t += 2.0 * S * (double)M * (double)N * 4.0 / hbm_bytes_per_us;
             if (best_t < 0 || t < best_t * 0.98) { best_t = t; best = MmPlan{S, cols}; }
@@ -609,31 +819,37 @@ MmPlan mm_plan(int qt, int64_t N, int64_t K, int64_t M) {
     return best;
 }
 
-int mm_ksplit(int qt, int64_t N, int64_t K, int64_t M) { return mm_plan(qt, N, K, M).S; }
+int mm_ksplit(int qt, int64_t N, int64_t K, int64_t M, bool cluster) { return mm_plan(qt, N, K, M, cluster).S; }
 
-// Partial buffers of the K splits are M*N binary32 each, padded to a multiple of 4 elements so that every
-// split starts 16-byte aligned.
+// Token columns per CTA of the plan (128, 256 or 512).
+int mm_plan_cols(int qt, int64_t N, int64_t K, int64_t M, bool cluster) { return mm_plan(qt, N, K, M, cluster).cols; }
+
+// Partial tiles of the K splits in scratch are M*N binary32 each, padded to a multiple of 4 elements so that
+// every split starts 16-byte aligned.
 static inline int64_t split_stride_of(int64_t M, int64_t N) { return (M * N + 3) & ~(int64_t)3; }
 
-// Bytes of split-K partials needed (0 when the K dimension is not split).
+// Bytes of scratch for the K splits' partial tiles (0 when the plan does not split K).
 size_t mm_partial_bytes(int qt, int64_t N, int64_t K, int64_t M) {
-    const int S = mm_ksplit(qt, N, K, M);
+    const int S = mm_ksplit(qt, N, K, M, false);
     return S > 1 ? (size_t)S * (size_t)split_stride_of(M, N) * 4 : 0;
 }
 
-// x_bf16: M x K bf16, row stride K*2 bytes (16-byte multiple), 16-byte aligned. `part` (when the K
-// dimension is split) holds S * M * N binary32.
-int launch_mm(int qt, int tile, const void *wq, int64_t N, int64_t K, const void *x_bf16, int64_t M, float *y,
-              float *part, unsigned int *status, cudaStream_t st) {
-    const MmPlan plan = mm_plan(qt, N, K, M);
+// x: M x K, bfloat16 (x_f32 false) or binary32 (x_f32 true, converted inside the kernel: the plan's columns
+// are then capped at 128), row stride a multiple of 16 bytes, 16-byte aligned. y: M x N binary32. `part`:
+// scratch of mm_partial_bytes() for the K splits' partial tiles (then the plan is the unclustered one), or
+// nullptr to add them inside a cluster (the clustered plan).
+int launch_mm(int qt, int tile, const void *wq, int64_t N, int64_t K, const void *x, bool x_f32, int64_t M,
+              float *y, float *part, unsigned int *status, cudaStream_t st) {
+    const MmPlan plan = mm_plan(qt, N, K, M, part == nullptr);
     const int S = plan.S;
+    const int cols = x_f32 && plan.cols > 128 ? 128 : plan.cols;
     const int64_t ksteps = (K + mm::BK - 1) / mm::BK;
     const int kps = (int)((ksteps + S - 1) / S);
-    float *out = S > 1 ? part : y;
+    if (S == 1) part = nullptr;
     const int64_t sstride = split_stride_of(M, N);
-    MmLaunch f{tile, tiles_per_cta(tile, M, plan.cols), wq, N, K, x_bf16, M, out, S, kps, sstride, status, st};
+    MmLaunch f{tile, tiles_per_cta(tile, M, cols), x_f32, wq, N, K, x, M, y, S, kps, part, sstride, status, st};
     int rc = dispatch_type(qt, f);
-    if (rc || S == 1) return rc;
+    if (rc || !part) return rc;
     const int64_t n = M * N, n4 = n / 4;
     if (n4 > 0) {
         int64_t blocks = (n4 + 255) / 256;
@@ -642,13 +858,13 @@ int launch_mm(int qt, int tile, const void *wq, int64_t N, int64_t K, const void
         float4 *y4 = reinterpret_cast<float4 *>(y);
         const int64_t s4 = sstride / 4;
         if (launch_pdl(reinterpret_cast<const void *>(mm::splitk_reduce_kernel), dim3((unsigned)blocks), dim3(256), 0,
-                       st, p4, s4, S, y4, n4))
+                       st, 1, p4, s4, S, y4, n4))
             return -6;
     }
     if (n % 4) {
         const float *pc = part;
         const int64_t beg = n4 * 4;
-        if (launch_pdl(reinterpret_cast<const void *>(mm::splitk_reduce_tail_kernel), dim3(1), dim3(32), 0, st, pc,
+        if (launch_pdl(reinterpret_cast<const void *>(mm::splitk_reduce_tail_kernel), dim3(1), dim3(32), 0, st, 1, pc,
                        sstride, S, y, beg, n))
             return -6;
     }
@@ -664,7 +880,7 @@ int launch_x_to_bf16(const float *x, void *out, int64_t n, cudaStream_t st) {
     const float4 *x4 = reinterpret_cast<const float4 *>(x);
     uint4 *o4 = static_cast<uint4 *>(out);
     return launch_pdl(reinterpret_cast<const void *>(mm::x_to_bf16_kernel), dim3((unsigned)blocks), dim3(threads), 0,
-                      st, x4, o4, n8);
+                      st, 1, x4, o4, n8);
 }
 
 }  // namespace wqk

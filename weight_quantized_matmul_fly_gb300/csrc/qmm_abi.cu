@@ -3,6 +3,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/qmm.h"
 #include "qmm_common.cuh"
 
@@ -17,10 +19,11 @@ int launch_gemv_tc(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, con
 int launch_gemv_tc_id(int qt, bool xbf16, const void *const *wq, int64_t E, int64_t N, int64_t K, const void *x,
                       bool x_per_slot, const int32_t *ids, int64_t M, int topk, float *y, unsigned int *status,
                       cudaStream_t st);
-int launch_mm(int qt, int tile, const void *wq, int64_t N, int64_t K, const void *x_bf16, int64_t M, float *y,
-              float *part, unsigned int *status, cudaStream_t st);
+int launch_mm(int qt, int tile, const void *wq, int64_t N, int64_t K, const void *x, bool x_f32, int64_t M,
+              float *y, float *part, unsigned int *status, cudaStream_t st);
 size_t mm_partial_bytes(int qt, int64_t N, int64_t K, int64_t M);
-int mm_ksplit(int qt, int64_t N, int64_t K, int64_t M);
+int mm_ksplit(int qt, int64_t N, int64_t K, int64_t M, bool cluster);
+int mm_plan_cols(int qt, int64_t N, int64_t K, int64_t M, bool cluster);
 int launch_x_to_bf16(const float *x, void *out, int64_t n, cudaStream_t st);
 int launch_mvid(int qt, bool xbf16, const void *const *wq, int64_t E, int64_t N, int64_t K, const void *x,
                 bool x_per_slot, const int32_t *ids, int64_t M, int topk, float *y, unsigned int *status,
@@ -54,17 +57,18 @@ int check_qmm(const void *wq, int qtype, int64_t N, int64_t K, const void *x, in
 // 16 bytes, and the decoders walk 32-weight chunks.
 inline bool mm_eligible(int qt, int64_t K) { return (K % 8) == 0 && (kQK[qt] >= 32 || K % 32 == 0); }
 
-// Device address of the status word on the current device (looked up once per device).
+// Device address of the status word on the current device (looked up once per device; host threads that
+// race on the first lookup all store the same address).
 unsigned int *status_ptr() {
-    static unsigned int *cache[64] = {};
+    static std::atomic<void *> cache[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!cache[dev]) {
-        void *p = nullptr;
+    void *p = cache[dev].load(std::memory_order_relaxed);
+    if (!p) {
         if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
-        cache[dev] = static_cast<unsigned int *>(p);
+        cache[dev].store(p, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return static_cast<unsigned int *>(p);
 }
 
 // The mat-vec path: quantized types on the tensor-core mat-vec kernel (16 tokens per launch at most,
@@ -99,35 +103,50 @@ int run_matvec(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const v
 
 inline size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
-// Scratch the tensor-core path needs: a bf16 copy of binary32 activations, then the binary32 partial
-// sums of the K splits when K is split over CTAs.
-size_t ws_x_bytes(int qtype, int64_t K, int64_t M) {
-    return (qtype & QMM_X_BF16) ? 0 : align256((size_t)M * (size_t)K * 2);
+// Binary32 activations on the tensor-core path. With scratch from the caller (qmm_ws) and more than 32
+// tokens, a separate pass writes a bf16 copy of x that the kernel loads by TMA at the plan's full width, and
+// a K split writes its partial tiles to the scratch for a second kernel to add. Otherwise (qmm and
+// qmm_with_tile, which take no scratch, and up to 32 tokens) the kernel converts x itself, with at most 128
+// columns per CTA, and adds a K split inside a thread block cluster. Measured on the Qwen3-Embedding-4B
+// projections: the conversion pass, chained to the kernel by programmatic dependent launch, costs 0.3-0.5 us
+// a call, converting inside the kernel 3-11 us at 64-128 columns but nothing at 32; behind the pass, a
+// cluster launch starts later than the second kernel costs; with bf16 activations the cluster is faster.
+// The two ways plan their K split separately (up to 32 CTAs, or up to 8 in a cluster), so qmm_ws and qmm
+// may differ in the last bits; each is the same for every token tile.
+bool f32_copy(int qtype, int64_t M, int path) { return path != 0 && !(qtype & QMM_X_BF16) && M > 32; }
+size_t ws_x_bytes(int qtype, int64_t K, int64_t M, int path) {
+    return f32_copy(qtype, M, path) ? align256((size_t)M * (size_t)K * 2) : 0;
 }
 size_t ws_bytes(int qtype, int64_t N, int64_t K, int64_t M, int path) {
-    if (path == 0) return 0;
-    return ws_x_bytes(qtype, K, M) + align256(mm_partial_bytes(qtype & 0xff, N, K, M));
+    if (!f32_copy(qtype, M, path)) return 0;
+    return ws_x_bytes(qtype, K, M, path) + align256(mm_partial_bytes(qtype & 0xff, N, K, M));
 }
 
 int run_mm(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, float *y, int tile,
            void *ws, size_t wsb, cudaStream_t st) {
     const int qt = qtype & 0xff;
-    const size_t need = ws_bytes(qtype, N, K, M, tile);
-    if (need && (!ws || wsb < need)) return QMM_EWORKSPACE;
     if (reinterpret_cast<uintptr_t>(ws) & 255u) return QMM_EALIGN;
-    const void *xb = x;
-    if (!(qtype & QMM_X_BF16)) {
-        int rc = launch_x_to_bf16(static_cast<const float *>(x), ws, M * K, st);
-        if (rc) return rc;
-        xb = ws;
-    }
-    float *part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ws_x_bytes(qtype, K, M));
     unsigned int *status = status_ptr();
     if (!status) return QMM_ECUDA;
-    return launch_mm(qt, tile, wq, N, K, xb, M, y, part, status, st);
+    const bool xf32 = !(qtype & QMM_X_BF16);
+    const size_t need = ws_bytes(qtype, N, K, M, tile);
+    if (need && ws && wsb >= need) {
+        int rc = launch_x_to_bf16(static_cast<const float *>(x), ws, M * K, st);
+        if (rc) return rc;
+        float *part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ws_x_bytes(qtype, K, M, tile));
+        return launch_mm(qt, tile, wq, N, K, ws, false, M, y, part, status, st);
+    }
+    return launch_mm(qt, tile, wq, N, K, x, xf32, M, y, nullptr, status, st);
 }
 
 }  // namespace
+
+namespace wqk {
+// The argument checks of qmm / qmm_ws, for the other entry points of the qmm family.
+int check_qmm_args(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, const float *y) {
+    return check_qmm(wq, qtype, N, K, x, M, y);
+}
+}  // namespace wqk
 
 extern "C" {
 
@@ -161,6 +180,8 @@ int qmm_ws(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int path = qmm_pick_path(qtype, N, K, M);
     if (path == 0) return run_matvec(qtype & 0xff, (qtype & QMM_X_BF16) != 0, wq, N, K, x, M, y, st);
+    const size_t need = ws_bytes(qtype, N, K, M, path);
+    if (need && (!workspace || workspace_bytes < need)) return QMM_EWORKSPACE;
     return run_mm(wq, qtype, N, K, x, M, y, path, workspace, workspace_bytes, st);
 }
 
@@ -170,14 +191,7 @@ int qmm(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int path = qmm_pick_path(qtype, N, K, M);
     if (path == 0) return run_matvec(qtype & 0xff, (qtype & QMM_X_BF16) != 0, wq, N, K, x, M, y, st);
-    const size_t need = ws_bytes(qtype, N, K, M, path);
-    void *ws = nullptr;
-    if (need) {
-        if (cudaMallocAsync(&ws, need, st) != cudaSuccess) return QMM_ECUDA;
-    }
-    rc = run_mm(wq, qtype, N, K, x, M, y, path, ws, need, st);
-    if (ws) cudaFreeAsync(ws, st);
-    return rc;
+    return run_mm(wq, qtype, N, K, x, M, y, path, nullptr, 0, st);
 }
 
 int qmm_with_tile(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, float *y, int tile,
@@ -188,14 +202,7 @@ int qmm_with_tile(const void *wq, int qtype, int64_t N, int64_t K, const void *x
     if (tile == 0) return run_matvec(qtype & 0xff, (qtype & QMM_X_BF16) != 0, wq, N, K, x, M, y, st);
     if (tile != 32 && tile != 64 && tile != 128) return QMM_ERANGE;
     if (!mm_eligible(qtype & 0xff, K)) return QMM_EBLOCK;
-    const size_t need = ws_bytes(qtype, N, K, M, tile);
-    void *ws = nullptr;
-    if (need) {
-        if (cudaMallocAsync(&ws, need, st) != cudaSuccess) return QMM_ECUDA;
-    }
-    rc = run_mm(wq, qtype, N, K, x, M, y, tile, ws, need, st);
-    if (ws) cudaFreeAsync(ws, st);
-    return rc;
+    return run_mm(wq, qtype, N, K, x, M, y, tile, nullptr, 0, st);
 }
 
 int qmm_id(const void *const *wq, int64_t E, int qtype, int64_t N, int64_t K, const void *x, const int32_t *ids,
@@ -269,6 +276,18 @@ int qmm_debug_stall(const void *wq, int qtype, int64_t N, int64_t K, const void 
                       nullptr, 1);
 }
 
+int qmm_plan_info(int qtype, int64_t N, int64_t K, int64_t M, int *ksplit, int *cols) {
+    if (!ksplit || !cols) return QMM_ENULL;
+    const int path = qmm_pick_path(qtype, N, K, M);
+    if (path < 0) return path;
+    if (path == 0) { *ksplit = 0; *cols = 0; return 0; }
+    if (N <= 0 || K <= 0 || M <= 0 || N >= kMaxDim || K >= kMaxDim || M >= kMaxDim) return QMM_EDIM;
+    const bool cluster = !f32_copy(qtype, M, path);
+    *ksplit = mm_ksplit(qtype & 0xff, N, K, M, cluster);
+    *cols = mm_plan_cols(qtype & 0xff, N, K, M, cluster);
+    return path;
+}
+
 int qmm_launch_count(int qtype, int64_t N, int64_t K, int64_t M) {
     const int path = qmm_pick_path(qtype, N, K, M);
     if (path < 0) return path;
@@ -280,8 +299,9 @@ int qmm_launch_count(int qtype, int64_t N, int64_t K, int64_t M) {
                                   nullptr, &n);
         return rc ? (int)((M + 15) / 16) : n;
     }
-    const int S = mm_ksplit(qtype & 0xff, N, K, M);
-    return ((qtype & QMM_X_BF16) ? 0 : 1) + 1 + (S > 1 ? 1 + ((M * N) % 4 ? 1 : 0) : 0);
+    if (!f32_copy(qtype, M, path)) return 1;
+    const int S = mm_ksplit(qtype & 0xff, N, K, M, false);
+    return 2 + (S > 1 ? 1 + ((M * N) % 4 ? 1 : 0) : 0);
 }
 
 const char *qmm_strerror(int code) {

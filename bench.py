@@ -1,18 +1,27 @@
-"""Benchmark: one Qwen3-Embedding-4B-shaped layer of block-quantized matmuls on one GB300.
+"""Benchmark: the block-quantized weight matmul on one GB300, over the five seeded synthetic workloads.
 
 A step is one pass of the whole hot path over the workload the pages time (candle PR 4056, "Metal:
 64-token tile for the quantized matrix-matrix kernel", section "This branch, kernel level"): the seven
-projections (attn_q/k/v/output Q4_K/Q6_K, ffn_gate/up Q4_K, ffn_down Q6_K) at every token count
-M in {1, 2, 7, 32, 33, 64, 96, 100, 128, 130, 136, 512, 2048}, plus the 65-token case as a batch of two
-sequences: 105 qmm calls. M <= 16 runs the mat-vec path, larger M the tcgen05 path.
+projections of one Qwen3-Embedding-4B layer (attn_q/k/v/output Q4_K/Q6_K, ffn_gate/up Q4_K, ffn_down Q6_K)
+at every token count M in {1, 2, 7, 32, 33, 64, 96, 100, 128, 130, 136, 512, 2048}, plus the 65-token case
+as a batch of two sequences: 105 qmm calls. M <= 16 runs the mat-vec path, larger M the tcgen05 path.
 
 Metric: weight-GB/s of the M <= 16 calls against HBM (value), and TFLOPS of the M >= 64 calls against the
 bf16 tensor-core peak (tflops_m_ge_64). Inputs are resident in HBM; weights rotate through 7 copies of the
 layer (447 MB, more than 3x the 129 MB L2) so that no call reads weights another call left in L2.
-The e2e figure times the same calls through the C-ABI with activations copied from pinned host memory and
+
+Roofline (per call): t_roof = max((weight + activation bytes) / HBM copy peak, 2 M N K / bf16 burst peak);
+a set of calls is at sum(t_roof) / sum(t_measured). Reported per class (M <= 16, 17..136, >= 512), for the
+whole step, and for the dominant kernel (the class that takes the most time).
+
+The other workloads are timed in the same run and reported as objects of the same JSON line: the small
+Q4_0 matrix at 1 and 7 tokens (small_q4_0), the Qwen3-0.6B-shaped decode layer with group-64 affine 4-bit
+weights (qwen3_06b), the expert-indexed product (moe) and the all-type sweep (sweep).
+The e2e figure times the M <= 16 calls through the C-ABI with activations copied from pinned host memory and
 results copied back inside the timed region.
 
     python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference] [--case NAME:M]
+                    [--no-cpu] [--no-moe] [--no-extra] [--detail]
 """
 from __future__ import annotations
 
@@ -44,21 +53,22 @@ WORKLOAD = ("Qwen3-Embedding-4B layer: attn_q 4096x2560 Q4_K, attn_k 1024x2560 Q
 
 
 # DRAM traffic per launch of the dominant kernel, from one ncu capture of the bench's own step
-# (`--steps 1 --warmup 3 --no-cpu --no-moe`): dram__bytes_read.sum + dram__bytes_write.sum averaged over the
-# 14 mm_kernel launches with M in {512, 2048}. Valid only for the kernel source it was taken on.
-MM_TRAFFIC = {"bytes_per_launch": 21.77e6, "launches": 14,
-              "source": "weight_quantized_matmul_fly_gb300/csrc/k_mm.cu",
-              "sha256": "17c5539d4901afcddfd6f414500e3b49cd920b09daca64bc9eb0ff831d0c036b"}
+# (dram__bytes_read.sum + dram__bytes_write.sum averaged over the kernel's launches in the class the
+# roofline object reports). Valid only for the kernel source it was taken on: None once that changed.
+TRAFFIC = {"class": None, "bytes_per_launch": None, "launches": 0,
+           "source": "weight_quantized_matmul_fly_gb300/csrc/k_mm.cu", "sha256": None}
 
 
-def mm_traffic():
-    """The recorded traffic per launch, or None when the kernel source changed since it was measured."""
+def recorded_traffic(cls):
+    """The recorded DRAM bytes per launch for this call class, or None (not measured on this source)."""
     import hashlib
+    if TRAFFIC["class"] != cls or not TRAFFIC["sha256"]:
+        return None
     try:
-        h = hashlib.sha256(open(os.path.join(ROOT, MM_TRAFFIC["source"]), "rb").read()).hexdigest()
+        h = hashlib.sha256(open(os.path.join(ROOT, TRAFFIC["source"]), "rb").read()).hexdigest()
     except OSError:
         return None
-    return MM_TRAFFIC["bytes_per_launch"] if h == MM_TRAFFIC["sha256"] else None
+    return TRAFFIC["bytes_per_launch"] if h == TRAFFIC["sha256"] else None
 
 
 def load_peaks():
@@ -68,6 +78,14 @@ def load_peaks():
         return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
                 "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def bench_config(world):
+    """The workload of a step, the same dict on both arms."""
+    return {"workload": WORKLOAD, "calls_per_step": len(calls_of_step()),
+            "l2": "rotating %d weight copies (%.0f MB), inputs larger than L2" % (
+                COPIES, COPIES * sum(weight_bytes(N, K, qt) for _, N, K, qt in LAYER) / 1e6),
+            "parallelism": "replicas" if world > 1 else "single GPU"}
 
 
 def calls_of_step():
@@ -168,6 +186,24 @@ def whole_job(pg, units_per_rank, seconds, world, device=None):
     """Whole-job throughput of N replicas doing the same work: the units all ranks processed divided by the
     slowest rank's time."""
     return units_per_rank * world / max_over_ranks(pg, seconds, device)
+
+
+def call_roofline(M, N, K, wbytes, x_elem_bytes, peaks):
+    """(roofline time in us, bound) of one call: max(bytes / HBM, flops / bf16 burst peak)."""
+    t_hbm = (wbytes + M * K * x_elem_bytes) / (peaks["hbm_gbs"] * 1e9) * 1e6
+    t_mma = 2.0 * M * N * K / (peaks["bf16_tflops"] * 1e12) * 1e6
+    return (t_hbm, "hbm") if t_hbm >= t_mma else (t_mma, "tensor")
+
+
+def class_summary(idx, calls, call_ms, rf, peaks):
+    t_meas = sum(call_ms[i] for i in idx) * 1e3
+    t_roof = sum(rf[i][0] for i in idx)
+    t_hbm = sum(rf[i][0] for i in idx if rf[i][1] == "hbm")
+    wb = sum(weight_bytes(calls[i][1], calls[i][2], calls[i][3]) for i in idx)
+    fl = sum(2.0 * calls[i][4] * calls[i][1] * calls[i][2] for i in idx)
+    return {"calls": len(idx), "us_measured": round(t_meas, 2), "us_roofline": round(t_roof, 2),
+            "frac": round(t_roof / t_meas, 4), "bound": "hbm" if t_hbm >= 0.5 * t_roof else "tensor",
+            "weight_gbs": round(wb / t_meas / 1e3, 1), "tflops": round(fl / t_meas / 1e6, 2)}
 
 
 # ---------------------------------------------------------------------------------------- our arm
@@ -295,37 +331,45 @@ def run_ours(args):
     gbs = whole_job(pg, wb_small, t_small, world, dev) / 1e9 if small else None
     tfl = whole_job(pg, fl_big, t_big, world, dev) / 1e12 if big else None
 
-    # dominant call class by time: the tensor-core calls at M >= 512 (or the mat-vec ones)
-    dom = [i for i, c in enumerate(calls) if c[4] >= 512]
-    if dom and sum(call_ms[i] for i in dom) >= sum(call_ms[i] for i in small):
-        fl = sum(2.0 * calls[i][4] * calls[i][1] * calls[i][2] for i in dom)
-        t = sum(call_ms[i] for i in dom) * 1e-3
-        ach = fl / t / 1e12
-        roof = {"bound": "tensor", "kernel": "mm_kernel (tcgen05) incl. its bf16 activation pre-pass",
-                "calls": "M in {512, 2048}", "achieved": round(ach, 2), "peak": peaks["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops_sustained"], 4),
-                "peak_kind": "bf16 sustained, %s" % peaks["source"], "traffic": mm_traffic(),
-                "traffic_unit": "DRAM bytes per mm_kernel launch (ncu, same calls)",
-                "algorithmic_per_launch": "2*M*N*K flops"}
-    else:
-        ach = wb_small / t_small / 1e9
-        roof = {"bound": "hbm", "kernel": "gemv_kernel", "calls": "M in {1, 2, 7}", "achieved": round(ach, 1),
-                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
-                "peak_kind": "HBM copy, %s" % peaks["source"], "traffic": None,
-                "algorithmic_per_launch": "N*K*bpw/8 weight bytes"}
+    # roofline per call, summed per class (group times: every group holds one token count, so a class,
+    # a set of token counts, is a union of groups and its measured time is exact)
+    rf = [call_roofline(c[4], c[1], c[2], weight_bytes(c[1], c[2], c[3]), 4, peaks) for c in calls]
+    classes = {"m_le_16": lambda m: m <= 16, "m_17_136": lambda m: 17 <= m <= 136, "m_ge_512": lambda m: m >= 512}
+    cls_out = {}
+    for name, pred in classes.items():
+        idx = [i for i, c in enumerate(calls) if pred(c[4])]
+        if not idx:
+            continue
+        cls_out[name] = class_summary(idx, calls, call_ms, rf, peaks)
+    step_summary = class_summary(list(range(ncalls)), calls, call_ms, rf, peaks)
+    dom = max(cls_out, key=lambda k: cls_out[k]["us_measured"])
+    d = cls_out[dom]
+    bound = d["bound"]
+    peak = peaks["hbm_gbs"] if bound == "hbm" else peaks["bf16_tflops"]
+    roof = {"bound": bound, "achieved": round(d["frac"] * peak, 2), "peak": peak,
+            "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "frac": d["frac"], "traffic": recorded_traffic(dom),
+            "class": dom, "kernel": ("gtc::gemv_tc_kernel (mma.sync mat-vec)" if dom == "m_le_16"
+                                     else "mm::mm_kernel (tcgen05) with its helper kernels"),
+            "peak_kind": ("HBM copy" if bound == "hbm" else "bf16 dense, burst") + ", " + peaks["source"],
+            "achieved_kind": "sum of per-call roofline times / measured time, times the peak of the bound "
+                             "that holds for most of the class's roofline time",
+            "algorithmic_per_call": "max((N*K*bpw/8 + M*K*4) / HBM, 2*M*N*K / bf16 peak)",
+            "traffic_unit": "DRAM bytes per launch of the kernel (ncu), null unless measured on this source"}
 
     per_m = {}
     for i, c in enumerate(calls):
         key = "%dx%d" % (2, c[4]) if c[4] == BATCH2 else str(c[4])
-        d = per_m.setdefault(key, {"us": 0.0, "wbytes": 0.0, "flops": 0.0})
+        d = per_m.setdefault(key, {"us": 0.0, "wbytes": 0.0, "flops": 0.0, "roof": 0.0})
         d["us"] += call_ms[i] * 1e3
         d["wbytes"] += weight_bytes(c[1], c[2], c[3])
         d["flops"] += 2.0 * c[4] * c[1] * c[2]
+        d["roof"] += rf[i][0]
     for k, d in per_m.items():
         d["weight_gbs"] = round(d["wbytes"] / (d["us"] * 1e-6) / 1e9, 1)
         d["tflops"] = round(d["flops"] / (d["us"] * 1e-6) / 1e12, 2)
+        d["frac"] = round(d["roof"] / d["us"], 4)
         d["us"] = round(d["us"], 2)
-        del d["wbytes"], d["flops"]
+        del d["wbytes"], d["flops"], d["roof"]
 
     if args.detail:
         for gi, (label, idxs) in enumerate(groups):
@@ -335,7 +379,13 @@ def run_ours(args):
                 label, len(idxs), group_ms[gi] * 1e3, wb / (group_ms[gi] * 1e-3) / 1e9,
                 fl / (group_ms[gi] * 1e-3) / 1e12), file=sys.stderr)
     e2e = run_e2e(args, qmm, torch, dev, calls, wq, ws) if not args.case else None
-    moe = run_moe(args, qmm, torch, dev) if (not args.case and not args.no_moe) else None
+    del wq, xs, ys, graphs
+    torch.cuda.empty_cache()
+    extra = not args.case and not args.no_extra
+    moe = run_moe(args, qmm, torch, dev, peaks) if (not args.case and not args.no_moe) else None
+    small_q4_0 = run_small_q4_0(qmm, torch, dev, peaks) if extra else None
+    qwen3_06b = run_qwen3_06b(qmm, torch, dev, peaks) if extra else None
+    sweep = run_sweep(qmm, torch, dev, peaks) if extra else None
     cpu = cpu_baseline(args) if (rank == 0 and world == 1 and not args.no_cpu and not args.case) else None
 
     clocks = clk.summary()
@@ -343,77 +393,208 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": round(gbs, 1) if gbs else None, "unit": "GB/s",
             "tflops_m_ge_64": {"value": round(tfl, 2) if tfl else None, "unit": "TFLOP/s",
-                               "frac_of_bf16_sustained": round(tfl / peaks["bf16_tflops_sustained"], 4) if tfl else None},
+                               "frac_of_bf16_burst": round(tfl / peaks["bf16_tflops"], 4) if tfl else None},
             "value_frac_of_hbm": round(gbs / peaks["hbm_gbs"] / world, 4) if gbs else None,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32 (M<=16) + bf16 in / f32 accumulate (M>16)", "data": "synthetic",
-            "config": {"workload": WORKLOAD if not args.case else "single call " + args.case,
-                       "calls_per_step": ncalls, "l2": "rotating %d weight copies (%.0f MB)" % (
-                           COPIES, COPIES * sum(weight_bytes(N, K, qt) for _, N, K, qt in LAYER) / 1e6),
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": per_step_launches * args.steps,
-            "clocks": clocks, "per_m": per_m, "moe": moe, "peaks": peaks,
+            "config": bench_config(world) if not args.case else {"workload": "single call " + args.case},
+            "roofline": roof, "roofline_classes": cls_out, "roofline_step": step_summary,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": per_step_launches * args.steps,
+            "clocks": clocks, "per_m": per_m, "small_q4_0": small_q4_0, "qwen3_06b": qwen3_06b, "moe": moe,
+            "sweep": sweep, "peaks": peaks,
         }
         print(json.dumps(line))
     if pg:
         pg.destroy_process_group()
 
 
-def run_moe(args, qmm, torch, dev):
+def time_graph(torch, stream, calls, replays=4):
+    """Device time per call (us) of the callables `calls`, captured back to back as one CUDA graph after
+    three eager warm-up passes and replayed `replays` times between two events on the launching stream."""
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            for f in calls:
+                f()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for f in calls:
+            f()
+    g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(replays):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (replays * len(calls))
+    del g
+    return us
+
+
+def quantized_copies(qmm, torch, dev, gen, qt, N, K, total_bytes):
+    """Copies of one N x K weight matrix (N(0, 0.02) from the seeded CUDA generator, quantized on the device)
+    whose total exceeds `total_bytes`, so that consecutive calls find nothing of theirs in L2."""
+    wbytes = qmm.row_bytes(qt, K) * N
+    bufs = []
+    for _ in range(max(2, int(total_bytes // wbytes) + 1)):
+        w = torch.randn(N, K, device=dev, generator=gen) * 0.02
+        b = torch.empty(wbytes, dtype=torch.uint8, device=dev)
+        qmm.qmm_quantize(w, qt, N, K, b)
+        bufs.append(b)
+        del w
+    return bufs
+
+
+def case_entry(M, N, K, wbytes, xb, us, peaks):
+    roof, bound = call_roofline(M, N, K, wbytes, xb, peaks)
+    return {"M": M, "us": round(us, 2), "weight_gbs": round(wbytes / us / 1e3, 1),
+            "tflops": round(2.0 * M * N * K / us / 1e6, 2), "frac": round(roof / us, 4), "bound": bound}
+
+
+def aggregate(cases, key_w="wbytes"):
+    t = sum(c["us"] for c in cases)
+    r = sum(c["frac"] * c["us"] for c in cases)
+    return round(r / t, 4) if t else None
+
+
+def run_moe(args, qmm, torch, dev, peaks):
     """The expert-indexed product on the MoE workload: 128 experts of 4096 x K Q4_0 (K in {512, 768, 1024}),
-    top-8 routing, n tokens in {1, 2, 4, 8, 12, 16, 24}; 16 id tables (8 distinct experts per token) rotate
-    between calls, and the experts total 151-302 MB per K, beyond the 129 MB L2 at K >= 768. Weights are
-    N(0, 0.02) from torch's seeded CUDA generator (timing only), quantized on the device. Metric: bytes of
-    the distinct experts each call streams / device time (CUDA events over a replayed graph of 32 calls)."""
-    E, N, TOPK, NB, REPS = synthetic.MOE_EXPERTS, synthetic.MOE_ROWS, synthetic.MOE_TOPK, 16, 32
+    top-8 routing, n tokens in {1, 2, 4, 8, 12, 16, 24}. Calls rotate through 64 id tables (8 distinct experts
+    per token) and 2 expert banks (2 x 128 experts, 302-604 MB per K), so no call finds its experts in L2.
+    Weights are N(0, 0.02) from torch's seeded CUDA generator (timing only), quantized on the device.
+    Metric: bytes of the distinct experts each call streams / device time (CUDA events over a replayed
+    graph of 64 calls); roofline per call as for the dense calls, with the distinct experts' bytes."""
+    E, N, TOPK, NT, NBANK = synthetic.MOE_EXPERTS, synthetic.MOE_ROWS, synthetic.MOE_TOPK, 64, 2
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
     stream = torch.cuda.Stream()
-    out, tot_b, tot_t = [], 0.0, 0.0
+    out, tot_b, tot_t, tot_r = [], 0.0, 0.0, 0.0
     for K in synthetic.MOE_K:
         rb = qmm.row_bytes("Q4_0", K)
-        wqs = []
-        for _ in range(E):
-            w = torch.randn(N, K, device=dev, generator=gen) * 0.02
-            b = torch.empty(rb * N, dtype=torch.uint8, device=dev)
-            qmm.qmm_quantize(w, "Q4_0", N, K, b)
-            wqs.append(b)
+        banks = []
+        for _ in range(NBANK):
+            bank = []
+            for _ in range(E):
+                w = torch.randn(N, K, device=dev, generator=gen) * 0.02
+                b = torch.empty(rb * N, dtype=torch.uint8, device=dev)
+                qmm.qmm_quantize(w, "Q4_0", N, K, b)
+                bank.append(b)
+            banks.append(bank)
         for n in synthetic.MOE_TOKENS:
-            tabs = [synthetic.expert_ids(n, batch=b) for b in range(NB)]
+            tabs = [synthetic.expert_ids(n, batch=b) for b in range(NT)]
             idss = [torch.from_numpy(t).to(dev) for t in tabs]
             distinct = [len(np.unique(t)) for t in tabs]
             x = torch.randn(n, K, device=dev, generator=gen)
             y = torch.empty(n, TOPK, N, device=dev)
-            with torch.cuda.stream(stream):
-                for i in range(3):
-                    qmm.qmm_id(wqs, "Q4_0", N, K, x, idss[i], y)
-            torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(REPS):
-                    qmm.qmm_id(wqs, "Q4_0", N, K, x, idss[i % NB], y)
-            g.replay()
-            torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                e0.record(stream)
-                for _ in range(4):
-                    g.replay()
-                e1.record(stream)
-            torch.cuda.synchronize()
-            us = e0.elapsed_time(e1) * 1e3 / (4 * REPS)
-            wbytes = float(np.mean([distinct[i % NB] for i in range(REPS)])) * rb * N
-            out.append({"K": K, "n": n, "us": round(us, 2), "weight_gbs": round(wbytes / us / 1e3, 1)})
+            fns = [(lambda i=i: qmm.qmm_id(banks[i % NBANK], "Q4_0", N, K, x, idss[i], y)) for i in range(NT)]
+            us = time_graph(torch, stream, fns)
+            wbytes = float(np.mean(distinct)) * rb * N
+            t_hbm = (wbytes + n * K * 4) / (peaks["hbm_gbs"] * 1e9) * 1e6
+            t_mma = 2.0 * n * TOPK * N * K / (peaks["bf16_tflops"] * 1e12) * 1e6
+            roof = max(t_hbm, t_mma)
+            out.append({"K": K, "n": n, "us": round(us, 2), "weight_gbs": round(wbytes / us / 1e3, 1),
+                        "frac": round(roof / us, 4)})
             tot_b += wbytes
             tot_t += us
-            del g
-        del wqs
+            tot_r += roof
+        del banks
+        torch.cuda.empty_cache()
     return {"metric": "expert-indexed weight-GB/s (distinct experts' bytes / time)", "unit": "GB/s",
-            "value": round(tot_b / tot_t / 1e3, 1),
-            "workload": "128 experts x 4096 x K Q4_0, top-8, K in {512,768,1024}, n in {1,2,4,8,12,16,24}",
-            "cases": out}
+            "value": round(tot_b / tot_t / 1e3, 1), "frac": round(tot_r / tot_t, 4),
+            "workload": "2 banks x 128 experts x 4096 x K Q4_0, top-8, K in {512,768,1024}, n in "
+                        "{1,2,4,8,12,16,24}; 64 id tables rotating", "cases": out}
+
+
+def run_small_q4_0(qmm, torch, dev, peaks):
+    """The small single-matrix workload: Q4_0 256 x 512, binary32 activations, 1 and 7 tokens. Its 73.7 KB of
+    weights would sit in L2, so calls rotate through 2048 copies (151 MB, beyond the 129 MB L2)."""
+    N, K = synthetic.SMALL_Q4_0
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    bufs = quantized_copies(qmm, torch, dev, gen, "Q4_0", N, K, 150e6)
+    stream = torch.cuda.Stream()
+    wbytes = qmm.row_bytes("Q4_0", K) * N
+    cases = []
+    for M in synthetic.SMALL_TOKENS:
+        x = torch.randn(M, K, device=dev, generator=gen)
+        y = torch.empty(M, N, device=dev)
+        us_all = []
+        for c0 in range(0, len(bufs), 256):
+            fns = [(lambda b=b: qmm.qmm(b, "Q4_0", N, K, x, y)) for b in bufs[c0:c0 + 256]]
+            us_all.append(time_graph(torch, stream, fns, replays=1))
+        cases.append(case_entry(M, N, K, wbytes, 4, float(np.mean(us_all)), peaks))
+    del bufs
+    return {"workload": "Q4_0 256x512, fp32 activations, M in {1,7}; 2048 rotating weight copies (151 MB)",
+            "cases": cases, "frac": aggregate(cases)}
+
+
+def run_qwen3_06b(qmm, torch, dev, peaks):
+    """The Qwen3-0.6B-shaped decode layer with group-64 affine 4-bit weights and bf16 activations: per token
+    count M in {1, 2, 4, 8, 16}, the seven projections and the output head as one group of calls (one CUDA
+    graph), weights rotating through 5 copies of the layer and head (483 MB). Metric: weight-GB/s."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    layer = synthetic.QWEN3_06B_LAYER
+    ncopy = 5
+    ws = {}
+    for c in range(ncopy):
+        for name, N, K, qt in layer:
+            w = torch.randn(N, K, device=dev, generator=gen) * 0.02
+            b = torch.empty(qmm.row_bytes(qt, K) * N, dtype=torch.uint8, device=dev)
+            qmm.qmm_quantize(w, qt, N, K, b)
+            ws[(c, name)] = b
+            del w
+    stream = torch.cuda.Stream()
+    groups, tot_b, tot_t, tot_r = [], 0.0, 0.0, 0.0
+    for M in synthetic.QWEN3_06B_TOKENS:
+        xs = {K: torch.randn(M, K, device=dev, generator=gen).to(torch.bfloat16) for K in {l[2] for l in layer}}
+        ys = {N: torch.empty(M, N, device=dev) for N in {l[1] for l in layer}}
+        fns = [(lambda c=c, name=name, N=N, K=K, qt=qt: qmm.qmm(ws[(c, name)], qt, N, K, xs[K], ys[N]))
+               for c in range(ncopy) for name, N, K, qt in layer]
+        us = time_graph(torch, stream, fns) * len(layer)          # per layer pass (8 calls)
+        wb = sum(qmm.row_bytes(qt, K) * N for _, N, K, qt in layer)
+        roof = sum(call_roofline(M, N, K, qmm.row_bytes(qt, K) * N, 2, peaks)[0] for _, N, K, qt in layer)
+        groups.append({"M": M, "us_per_layer": round(us, 2), "weight_gbs": round(wb / us / 1e3, 1),
+                       "frac": round(roof / us, 4)})
+        tot_b += wb
+        tot_t += us
+        tot_r += roof
+    del ws
+    return {"workload": "Qwen3-0.6B layer (q,k,v,o,gate,up,down) + lm_head 151936x1024, A4G64, bf16 "
+                        "activations, M in {1,2,4,8,16}; 5 rotating copies (483 MB)",
+            "value": round(tot_b / tot_t / 1e3, 1), "unit": "GB/s", "frac": round(tot_r / tot_t, 4),
+            "groups": groups}
+
+
+def run_sweep(qmm, torch, dev, peaks):
+    """The all-type sweep on one ffn_gate-shaped 9728 x 2560 matrix, binary32 activations, M in {1, 16, 64,
+    512, 2048}; per type, rotating weight copies beyond 3x L2 (400 MB); 20 calls per graph."""
+    N, K = synthetic.SWEEP_SHAPE
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    stream = torch.cuda.Stream()
+    out, allc = {}, []
+    for qt in synthetic.SWEEP_TYPES:
+        bufs = quantized_copies(qmm, torch, dev, gen, qt, N, K, 400e6)
+        wbytes = qmm.row_bytes(qt, K) * N
+        cases = []
+        for M in synthetic.SWEEP_TOKENS:
+            x = torch.randn(M, K, device=dev, generator=gen)
+            y = torch.empty(M, N, device=dev)
+            ws = torch.empty(max(256, qmm.qmm_workspace_size(qt, N, K, M)), dtype=torch.uint8, device=dev)
+            fns = [(lambda b=bufs[i % len(bufs)]: qmm.qmm_ws(b, qt, N, K, x, y, ws)) for i in range(20)]
+            cases.append(case_entry(M, N, K, wbytes, 4, time_graph(torch, stream, fns), peaks))
+        out[qt] = cases
+        allc += cases
+        del bufs
+        torch.cuda.empty_cache()
+    return {"workload": "ffn_gate 9728x2560, 13 types, fp32 activations, M in {1,16,64,512,2048}",
+            "frac": aggregate(allc), "types": out}
 
 
 def run_e2e(args, qmm, torch, dev, calls, wq, ws):
@@ -477,73 +658,6 @@ def run_e2e(args, qmm, torch, dev, calls, wq, ws):
                      "device-to-host copy of their results per step, replayed as CUDA graphs"}
 
 
-def run_extra(args):
-    """The other workloads, timed per call (not part of the bench line): the all-type sweep on one
-    9728 x 2560 matrix (fp32 activations, M in {1, 16, 64, 512, 2048}) and the Qwen3-0.6B-shaped calls with
-    group-64 affine 4-bit weights (bf16 activations, M in {1, 2, 4, 8, 16}). Each case: weights quantized on
-    the device from torch's seeded CUDA generator (timing only), enough copies to exceed L2, 20 calls per
-    CUDA graph replayed 4 times. Prints one JSON line."""
-    import torch
-    import weight_quantized_matmul_fly_gb300 as qmm
-    qmm.build()
-    dev = torch.device("cuda")
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(0)
-    stream = torch.cuda.Stream()
-
-    def time_case(qt, N, K, Ms, bf16):
-        wbytes = qmm.row_bytes(qt, K) * N
-        ncopy = max(2, int(300e6 // wbytes) + 1)
-        bufs = []
-        for _ in range(ncopy):
-            w = torch.randn(N, K, device=dev, generator=gen) * 0.02
-            b = torch.empty(wbytes, dtype=torch.uint8, device=dev)
-            qmm.qmm_quantize(w, qt, N, K, b)
-            bufs.append(b)
-            del w
-        out = []
-        for M in Ms:
-            x = torch.randn(M, K, device=dev, generator=gen)
-            if bf16:
-                x = x.to(torch.bfloat16)
-            y = torch.empty((M, N), dtype=torch.float32, device=dev)
-            ws = torch.empty(max(256, qmm.qmm_workspace_size(qt, N, K, M)), dtype=torch.uint8, device=dev)
-            with torch.cuda.stream(stream):
-                for i in range(3):
-                    qmm.qmm_ws(bufs[i % ncopy], qt, N, K, x, y, ws)
-            torch.cuda.synchronize()
-            reps = 20
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(reps):
-                    qmm.qmm_ws(bufs[i % ncopy], qt, N, K, x, y, ws)
-            g.replay()
-            torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                e0.record(stream)
-                for _ in range(4):
-                    g.replay()
-                e1.record(stream)
-            torch.cuda.synchronize()
-            us = e0.elapsed_time(e1) * 1e3 / (4 * reps)
-            out.append({"M": M, "us": round(us, 2), "weight_gbs": round(wbytes / us / 1e3, 1),
-                        "tflops": round(2.0 * M * N * K / us / 1e6, 2)})
-            del g
-        del bufs
-        return out
-
-    sweep = {}
-    N, K = synthetic.SWEEP_SHAPE
-    for qt in synthetic.SWEEP_TYPES:
-        sweep[qt] = time_case(qt, N, K, synthetic.SWEEP_TOKENS, False)
-    q06 = {}
-    for name, N, K, qt in synthetic.QWEN3_06B_LAYER:
-        q06[name] = time_case(qt, N, K, synthetic.QWEN3_06B_TOKENS, True)
-    print(json.dumps({"extra": True, "sweep_9728x2560": sweep, "qwen3_06b_a4g64": q06}))
-
-
 # ---------------------------------------------------------------------------------------- oracle legs
 
 def oracle_step_sample():
@@ -558,28 +672,39 @@ def oracle_step_sample():
 
 
 def time_oracle_sample(oracle, ws, xs):
-    t0 = time.perf_counter()
+    """One pass of the oracle over the sample: every call's weights decoded to binary64 (dequant), then the
+    product (matmul), the two steps timed separately. Returns (weight bytes, dequant s, matmul s)."""
+    td = tm = 0.0
     wb = 0.0
     for M in (1, 2, 7):
         for name, N, K, qt in LAYER:
-            oracle.qmm(qt, ws[name], N, K, xs[(M, K)])
+            t0 = time.perf_counter()
+            W = oracle.dequant_f64(qt, ws[name], N, K)
+            t1 = time.perf_counter()
+            oracle.matmul_f64(W, xs[(M, K)])
+            t2 = time.perf_counter()
+            td += t1 - t0
+            tm += t2 - t1
             wb += weight_bytes(N, K, qt)
-    return wb, time.perf_counter() - t0
+    return wb, td, tm
 
 
 def cpu_baseline(args, seconds=10.0):
     """The oracle on the step's 21 M<=16 calls, passes repeated for about `seconds` of CPU work."""
     oracle, ws, xs = oracle_step_sample()
-    wb = t = 0.0
+    wb = td = tm = 0.0
     passes = 0
-    while passes == 0 or t < seconds:
-        b, dt = time_oracle_sample(oracle, ws, xs)
+    while passes == 0 or td + tm < seconds:
+        b, d, m = time_oracle_sample(oracle, ws, xs)
         wb += b
-        t += dt
+        td += d
+        tm += m
         passes += 1
+    t = td + tm
     return {"value": round(wb / t / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": "the 21 calls with M<=16 (7 projections x M in {1,2,7}), full outputs, %d passes (%.1f s)" % (
-                passes, t)}
+            "dequant_s": round(td, 3), "matmul_s": round(tm, 3),
+            "sample": "the 21 calls with M<=16 (7 projections x M in {1,2,7}), full outputs, %d passes (%.1f s: "
+                      "dequant %.1f s, matmul %.1f s)" % (passes, t, td, tm)}
 
 
 def run_reference(args):
@@ -591,19 +716,23 @@ def run_reference(args):
     for _ in range(args.warmup):
         time_oracle_sample(oracle, ws, xs)
     t0 = time.perf_counter()
-    wb = 0.0
+    wb = td = tm = 0.0
     for _ in range(args.steps):
-        b, _t = time_oracle_sample(oracle, ws, xs)
+        b, d, m = time_oracle_sample(oracle, ws, xs)
         wb += b
+        td += d
+        tm += m
     t = time.perf_counter() - t0
     v = wb / t / 1e9
     cores = oracle.num_threads()
-    sample = "per step: the 21 calls with M<=16 of the layer (7 projections x M in {1,2,7}), full outputs"
+    sample = ("per step: the 21 calls with M<=16 of the layer (7 projections x M in {1,2,7}), full outputs; "
+              "dequant %.2f s, matmul %.2f s over the run" % (td, tm))
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "sample": sample},
-            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "config": bench_config(world),
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
+                             "dequant_s": round(td, 3), "matmul_s": round(tm, 3)},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -618,14 +747,12 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--detail", action="store_true", help="per-call device times on stderr")
     ap.add_argument("--no-moe", action="store_true", help="skip the expert-indexed (MoE) leg")
-    ap.add_argument("--extra", action="store_true",
-                    help="instead of the bench line: time the all-type sweep and the Qwen3-0.6B shapes")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the small Q4_0, Qwen3-0.6B and all-type sweep objects")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.extra:
-        run_extra(args)
-    elif args.impl == "reference":
+    if args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -159,6 +159,20 @@ int qmm_noalloc(const void *wq, int qtype, int64_t N, int64_t K, const void *x, 
 int qmm_id(const void *const *wq, int64_t E, int qtype, int64_t N, int64_t K, const void *x,
            const int32_t *ids, int64_t M, int topk, float *y, void *stream);
 
+/* Which kernel qmm_id runs (qmm_id_pick_path): 1 = the expert-indexed mat-vec (binary32 products of the
+ * exactly rounded weights, tolerance class 1e-5), used while an expert gets few routed pairs on average
+ * (M*topk < 16 * min(E, M*topk)); 2 = the tensor-core expert kernel (x and weights rounded to bfloat16,
+ * tolerance class 4e-3, like qmm's tensor-core path): each CTA takes one row block of one distinct expert
+ * and runs tcgen05 MMAs over passes of up to 32/64/128 of its routed pairs, the activation rows gathered
+ * by bulk copies, so each pass decodes the expert's weights once for all of them. Path 2 needs K a
+ * multiple of 8 (plain types: 32). */
+int qmm_id_pick_path(int qtype, int64_t E, int64_t K, int64_t M, int topk);
+
+/* qmm_id with the path forced (tests and diagnostics): path 0 = as qmm_id picks, 1 or 2 as above.
+ * QMM_ERANGE for another value. */
+int qmm_id_with_path(const void *const *wq, int64_t E, int qtype, int64_t N, int64_t K, const void *x,
+                     const int32_t *ids, int64_t M, int topk, float *y, int path, void *stream);
+
 /*
  * qmm_with_tile: qmm() with the path forced, for tests and diagnostics (mirrors the pages' explicit-tile
  * entry point, candle PR 4056, section "What changes").

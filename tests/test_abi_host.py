@@ -137,3 +137,13 @@ def test_noalloc_checks_arguments_first(L):
     # a null x with a large M is a null pointer, not an oversized workspace
     assert L.qmm_noalloc(P(A), 3, 64, 8192, None, 1 << 20, P(A), None) == -4
     assert L.qmm_noalloc(P(A), 3, 64, -64, P(A), 1 << 20, P(A), None) == -3
+
+
+def test_qmm_id_path_choice(L):
+    # a few pairs per expert: the mat-vec expert kernel; many (prefill): the tensor-core one
+    assert qmm.qmm_id_pick_path("Q4_0", 128, 512, 24, 8) == 1
+    assert qmm.qmm_id_pick_path("Q4_0", 128, 512, 256, 8) == 2
+    assert qmm.qmm_id_pick_path("F32", 8, 256, 64, 2) == 2
+    ptrs = (ctypes.c_void_p * 2)(A, A)
+    arr = ctypes.cast(ptrs, P)
+    assert L.qmm_id_with_path(arr, 2, 3, 64, 64, P(A), P(A), 1, 8, P(A), 3, None) == -7   # no such path

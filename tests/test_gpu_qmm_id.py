@@ -78,14 +78,20 @@ def test_qmm_id_long_k_cluster_split():
 
 @pytest.mark.parametrize("bf16", [False, True])
 def test_qmm_id_many_slots_per_expert(bf16):
-    """64 tokens over 4 experts (about 64 slots each): many passes of 4 (8 for bf16 activations) tokens."""
+    """64 tokens over 4 experts (about 64 slots each). qmm_id picks the tensor-core expert kernel there
+    (bf16 class); forced onto the mat-vec expert kernel the call runs many passes of 4 (8 for bf16
+    activations) tokens (binary32 class)."""
+    from gpu_util import TOL_BF16
     E, N, K, M, topk = 4, 96, 512, 64, 4
     wqs = _experts("Q4_K", E, N, K, seed=5)
     x = synthetic.activations(M, K, seed=5, bf16=bf16)
     ids = synthetic.expert_ids(M, E=E, topk=topk, seed=5)
-    y = _run(wqs, "Q4_K", N, K, x, ids)
     ref, bnd = oracle.qmm_id("Q4_K", wqs, N, K, x, ids)
-    check_tol(y, ref, bnd, TOL_FP32, "many slots bf16=%s" % bf16)
+    assert qmm.qmm_id_pick_path("Q4_K", E, K, M, topk) == 2
+    y = _run(wqs, "Q4_K", N, K, x, ids)
+    check_tol(y, ref, bnd, TOL_BF16, "many slots, auto, bf16=%s" % bf16)
+    y1 = _run_path(wqs, "Q4_K", N, K, x, ids, 1)
+    check_tol(y1, ref, bnd, TOL_FP32, "many slots, mat-vec, bf16=%s" % bf16)
 
 
 @pytest.mark.parametrize("qtype", ["Q4_0", "Q4_K", "Q6_K", "A4G64", "F16", "BF16"])
@@ -100,9 +106,75 @@ def test_qmm_id_per_slot_activations(qtype, M):
     ids = synthetic.expert_ids(M, E=E, topk=topk, seed=M + 60)
     y = _run(wqs, qtype, N, K, x, ids)
     ref, bnd = oracle.qmm_id(qtype, wqs, N, K, x, ids)
-    check_tol(y, ref, bnd, TOL_FP32, "%s per-slot M=%d" % (qtype, M))
+    from gpu_util import TOL_BF16
+    tol = TOL_BF16 if qmm.qmm_id_pick_path(qtype, E, K, M, topk) == 2 else TOL_FP32
+    check_tol(y, ref, bnd, tol, "%s per-slot M=%d" % (qtype, M))
     # the broadcast form is the per-slot form with every slot given its token's row
     xb = synthetic.activations(M, K, seed=M + 61, bf16=bf16)
     y1 = _run(wqs, qtype, N, K, xb, ids)
     y2 = _run(wqs, qtype, N, K, np.ascontiguousarray(np.repeat(xb[:, None, :], topk, axis=1)), ids)
     assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+
+
+# ------------------------------------------------------------------ tensor-core expert path (many pairs per expert)
+
+def _run_path(wqs, qtype, N, K, x, ids, path):
+    torch = torch_cuda()
+    M, topk = ids.shape
+    y = torch.full((M, topk, N), float("nan"), dtype=torch.float32, device="cuda")
+    qmm.qmm_id([dev(w) for w in wqs], qtype, N, K, x_dev(x), dev(ids), y, path=path)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("n", [32, 64, 256])
+def test_qmm_id_tensor_core_128_experts(n):
+    """Prefill-sized routing (llama.cpp PR 28086, "Test methodology": MUL_MAT_ID): n tokens, top-8 of 128
+    experts, on the tensor-core expert kernel, element by element against the oracle (bf16 class), and
+    the mat-vec expert kernel on the same inputs (binary32 class)."""
+    from gpu_util import TOL_BF16
+    E, N, K, topk = 128, 256, 512, 8
+    wqs = _experts("Q4_0", E, N, K, seed=700)
+    x = synthetic.activations(n, K, seed=n)
+    ids = synthetic.expert_ids(n, E=E, topk=topk, seed=n)
+    ref, bnd = oracle.qmm_id("Q4_0", wqs, N, K, x, ids)
+    y2 = _run_path(wqs, "Q4_0", N, K, x, ids, 2)
+    check_tol(y2, ref, bnd, TOL_BF16, "tensor-core n=%d" % n)
+    y1 = _run_path(wqs, "Q4_0", N, K, x, ids, 1)
+    check_tol(y1, ref, bnd, TOL_FP32, "mat-vec n=%d" % n)
+    assert qmm.qmm_id_pick_path("Q4_0", E, K, n, topk) == (2 if n * topk >= 16 * min(E, n * topk) else 1)
+
+
+@pytest.mark.parametrize("qtype", ["Q4_K", "Q6_K", "Q8_0", "A4G64", "Q5_1", "F16", "F32"])
+def test_qmm_id_tensor_core_types_and_passes(qtype):
+    """Few experts and many tokens, so that experts get more pairs than one pass holds (several passes
+    into the same accumulator), with a duplicate id and ragged rows."""
+    from gpu_util import TOL_BF16
+    E, N, K, M, topk = 4, 200, 512, 150, 2
+    wqs = _experts(qtype, E, N, K, seed=800)
+    bf16 = qtype == "A4G64"
+    x = synthetic.activations(M, K, seed=8, bf16=bf16)
+    ids = synthetic.expert_ids(M, E=E, topk=topk, seed=8)
+    ids[3] = [1, 1]
+    ref, bnd = oracle.qmm_id(qtype, wqs, N, K, x, ids)
+    y = _run_path(wqs, qtype, N, K, x, ids, 2)
+    check_tol(y, ref, bnd, TOL_BF16, qtype)
+    assert qmm.qmm_id_pick_path(qtype, E, K, M, topk) == 2
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_qmm_id_tensor_core_per_slot_and_k_tail(bf16):
+    """Per-slot activation rows (M x topk x K) and K = 96 (the last K step half full), plus bad ids."""
+    from gpu_util import TOL_BF16
+    torch_cuda()
+    E, N, K, M, topk = 6, 130, 96, 40, 3
+    wqs = _experts("Q4_0", E, N, K, seed=900)
+    x = synthetic.activations(M * topk, K, seed=9, bf16=bf16).reshape(M, topk, K)
+    ids = synthetic.expert_ids(M, E=E, topk=topk, seed=9)
+    ids[5, 1] = 77
+    ids[7, 0] = -2
+    qmm.qmm_get_status()
+    y = _run_path(wqs, "Q4_0", N, K, x, ids, 2)
+    assert qmm.qmm_get_status() & qmm.STATUS_BAD_ID
+    ref, bnd = oracle.qmm_id("Q4_0", wqs, N, K, x, ids)
+    check_tol(y, ref, bnd, TOL_BF16, "per-slot bf16=%s" % bf16)

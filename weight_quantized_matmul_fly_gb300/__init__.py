@@ -13,7 +13,7 @@ import os
 
 __all__ = ["QmmError", "TYPES", "TYPE_ID", "X_BF16", "X_PER_SLOT", "build", "lib", "qmm", "qmm_ws", "qmm_workspace_size",
            "qmm_launch_count", "qmm_plan_info", "qmm_noalloc", "NOALLOC_SCRATCH_BYTES",
-           "qmm_id", "qmm_with_tile", "qmm_pick_tile", "qmm_pick_path", "qmm_dequant", "qmm_quantize",
+           "qmm_id", "qmm_id_with_path", "qmm_id_pick_path", "qmm_with_tile", "qmm_pick_tile", "qmm_pick_path", "qmm_dequant", "qmm_quantize",
            "qmm_type_info", "qmm_get_status", "qmm_debug_stall", "qmm_strerror", "row_bytes", "EXPORTS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -27,7 +27,8 @@ X_PER_SLOT = 0x200
 STATUS_BAD_ID, STATUS_TIMEOUT = 0x1, 0x2
 
 # Every symbol include/qmm.h declares.
-EXPORTS = ["qmm", "qmm_ws", "qmm_workspace_size", "qmm_noalloc", "qmm_id", "qmm_with_tile", "qmm_pick_tile",
+EXPORTS = ["qmm", "qmm_ws", "qmm_workspace_size", "qmm_noalloc", "qmm_id", "qmm_id_with_path", "qmm_id_pick_path",
+           "qmm_with_tile", "qmm_pick_tile",
            "qmm_pick_path", "qmm_launch_count", "qmm_plan_info", "qmm_dequant", "qmm_quantize", "qmm_type_info", "qmm_get_status",
            "qmm_debug_stall", "qmm_strerror"]
 NOALLOC_SCRATCH_BYTES = 64 << 20   # QMM_NOALLOC_SCRATCH_BYTES
@@ -61,6 +62,8 @@ def lib():
             "qmm_noalloc": ([P, I, I64, I64, P, I64, P, P], I),
             "qmm_workspace_size": ([I, I64, I64, I64], SZ),
             "qmm_id": ([P, I64, I, I64, I64, P, P, I64, I, P, P], I),
+            "qmm_id_with_path": ([P, I64, I, I64, I64, P, P, I64, I, P, I, P], I),
+            "qmm_id_pick_path": ([I, I64, I64, I64, I], I),
             "qmm_with_tile": ([P, I, I64, I64, P, I64, P, I, P], I),
             "qmm_pick_tile": ([I64], I),
             "qmm_pick_path": ([I, I64, I64, I64], I),
@@ -186,16 +189,26 @@ def qmm_with_tile(wq, qtype, N: int, K: int, x, y, tile: int, stream=None):
     return y
 
 
-def qmm_id(wqs, qtype, N: int, K: int, x, ids, y, stream=None):
+def qmm_id(wqs, qtype, N: int, K: int, x, ids, y, stream=None, path: int = 0):
     """y[M, topk, N]: for each token t and slot j, x[t] @ dequant(wqs[ids[t, j]])^T; x of shape (M, K), or
-    (M, topk, K) for one activation row per (token, slot), which is then x[t, j]."""
+    (M, topk, K) for one activation row per (token, slot), which is then x[t, j]. path 0 lets the library
+    pick the kernel (qmm_id); 1 / 2 force the mat-vec / tensor-core expert kernel (qmm_id_with_path)."""
     M, topk = ids.shape
     flags = _xflag(x) | (X_PER_SLOT if x.dim() == 3 else 0)
     arr = (ctypes.c_void_p * len(wqs))(*[w.data_ptr() for w in wqs])
-    rc = lib().qmm_id(ctypes.cast(arr, ctypes.c_void_p), len(wqs), _qt(qtype) | flags, int(N), int(K),
-                      _ptr(x), _ptr(ids), int(M), int(topk), _ptr(y), _stream(stream))
+    if path == 0:
+        rc = lib().qmm_id(ctypes.cast(arr, ctypes.c_void_p), len(wqs), _qt(qtype) | flags, int(N), int(K),
+                          _ptr(x), _ptr(ids), int(M), int(topk), _ptr(y), _stream(stream))
+    else:
+        rc = lib().qmm_id_with_path(ctypes.cast(arr, ctypes.c_void_p), len(wqs), _qt(qtype) | flags, int(N),
+                                    int(K), _ptr(x), _ptr(ids), int(M), int(topk), _ptr(y), int(path),
+                                    _stream(stream))
     _check(rc, "qmm_id")
     return y
+
+
+def qmm_id_pick_path(qtype, E: int, K: int, M: int, topk: int) -> int:
+    return lib().qmm_id_pick_path(_qt(qtype), int(E), int(K), int(M), int(topk))
 
 
 def qmm_dequant(wq, qtype, N: int, K: int, w_out, stream=None):

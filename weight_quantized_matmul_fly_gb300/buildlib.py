@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "libqmm.so")
 BUILD = os.path.join(ROOT, "_build")
 
-SOURCES = ["qmm_abi.cu", "k_dequant.cu", "k_gemv.cu", "k_gemv_tc.cu", "k_mm.cu", "k_mvid.cu", "qmm_noalloc.cu"]
+SOURCES = ["qmm_abi.cu", "k_dequant.cu", "k_gemv.cu", "k_gemv_tc.cu", "k_mm.cu", "k_mm_id.cu", "k_mvid.cu",
+           "qmm_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-v"]

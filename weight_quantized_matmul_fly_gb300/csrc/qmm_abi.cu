@@ -25,6 +25,9 @@ size_t mm_partial_bytes(int qt, int64_t N, int64_t K, int64_t M);
 int mm_ksplit(int qt, int64_t N, int64_t K, int64_t M, bool cluster);
 int mm_plan_cols(int qt, int64_t N, int64_t K, int64_t M, bool cluster);
 int launch_x_to_bf16(const float *x, void *out, int64_t n, cudaStream_t st);
+int launch_mm_id(int qt, bool xbf16, const void *const *wq, int64_t E, int64_t N, int64_t K, const void *x,
+                 bool x_per_slot, const int32_t *ids, int64_t M, int topk, float *y, unsigned int *status,
+                 cudaStream_t st);
 int launch_mvid(int qt, bool xbf16, const void *const *wq, int64_t E, int64_t N, int64_t K, const void *x,
                 bool x_per_slot, const int32_t *ids, int64_t M, int topk, float *y, unsigned int *status,
                 cudaStream_t st);
@@ -139,6 +142,44 @@ int run_mm(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64
     return launch_mm(qt, tile, wq, N, K, x, xf32, M, y, nullptr, status, st);
 }
 
+// Expert-indexed path for the routing a call carries on average: the tensor-core kernel once an expert
+// gets enough routed pairs that decoding its weights once per pass of up to 32-128 pairs beats the mat-vec
+// machinery's passes of 4 (8 with bf16 activations) pairs.
+constexpr int64_t kIdTensorMinPairs = 16;
+int pick_id_path(int qt, int64_t E, int64_t K, int64_t M, int topk) {
+    const int64_t nslot = M * topk, used = nslot < E ? nslot : E;
+    return (mm_eligible(qt, K) && nslot >= kIdTensorMinPairs * used) ? 2 : 1;
+}
+
+int run_qmm_id(const void *const *wq, int64_t E, int qtype, int64_t N, int64_t K, const void *x, const int32_t *ids,
+               int64_t M, int topk, float *y, void *stream, int path) {
+    if ((qtype & ~(0xff | QMM_X_BF16 | QMM_X_PER_SLOT)) != 0) return QMM_EQTYPE;
+    const int qt = qtype & 0xff;
+    if (qt < 0 || qt >= T_COUNT) return QMM_EQTYPE;
+    if (N <= 0 || K <= 0 || M <= 0 || N >= kMaxDim || K >= kMaxDim) return QMM_EDIM;
+    if (K % kQK[qt] != 0 || K % 32 != 0) return QMM_EBLOCK;
+    if (E < 1 || E > QMM_MAX_EXPERTS || topk < 1 || M * (int64_t)topk > QMM_MAX_ID_SLOTS) return QMM_ERANGE;
+    if (path < 0 || path > 2) return QMM_ERANGE;
+    if (!wq || !x || !ids || !y) return QMM_ENULL;
+    for (int64_t e = 0; e < E; ++e) {
+        if (!wq[e]) return QMM_ENULL;
+        if (!aligned16(wq[e])) return QMM_EALIGN;
+    }
+    if (!aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(ids) & 3u)) return QMM_EALIGN;
+    unsigned int *status = status_ptr();
+    if (!status) return QMM_ECUDA;
+    const bool xbf16 = (qtype & QMM_X_BF16) != 0, per_slot = (qtype & QMM_X_PER_SLOT) != 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (path == 0) path = pick_id_path(qt, E, K, M, topk);
+    if (path == 2) {
+        if (!mm_eligible(qt, K)) return QMM_EBLOCK;
+        return launch_mm_id(qt, xbf16, wq, E, N, K, x, per_slot, ids, M, topk, y, status, st);
+    }
+    const int rc = launch_gemv_tc_id(qt, xbf16, wq, E, N, K, x, per_slot, ids, M, topk, y, status, st);
+    if (rc != -3) return rc;
+    return launch_mvid(qt, xbf16, wq, E, N, K, x, per_slot, ids, M, topk, y, status, st);
+}
+
 }  // namespace
 
 namespace wqk {
@@ -207,26 +248,19 @@ int qmm_with_tile(const void *wq, int qtype, int64_t N, int64_t K, const void *x
 
 int qmm_id(const void *const *wq, int64_t E, int qtype, int64_t N, int64_t K, const void *x, const int32_t *ids,
            int64_t M, int topk, float *y, void *stream) {
-    if ((qtype & ~(0xff | QMM_X_BF16 | QMM_X_PER_SLOT)) != 0) return QMM_EQTYPE;
+    return run_qmm_id(wq, E, qtype, N, K, x, ids, M, topk, y, stream, 0);
+}
+
+int qmm_id_with_path(const void *const *wq, int64_t E, int qtype, int64_t N, int64_t K, const void *x,
+                     const int32_t *ids, int64_t M, int topk, float *y, int path, void *stream) {
+    return run_qmm_id(wq, E, qtype, N, K, x, ids, M, topk, y, stream, path);
+}
+
+int qmm_id_pick_path(int qtype, int64_t E, int64_t K, int64_t M, int topk) {
     const int qt = qtype & 0xff;
     if (qt < 0 || qt >= T_COUNT) return QMM_EQTYPE;
-    if (N <= 0 || K <= 0 || M <= 0 || N >= kMaxDim || K >= kMaxDim) return QMM_EDIM;
-    if (K % kQK[qt] != 0 || K % 32 != 0) return QMM_EBLOCK;
-    if (E < 1 || E > QMM_MAX_EXPERTS || topk < 1 || M * (int64_t)topk > QMM_MAX_ID_SLOTS) return QMM_ERANGE;
-    if (!wq || !x || !ids || !y) return QMM_ENULL;
-    for (int64_t e = 0; e < E; ++e) {
-        if (!wq[e]) return QMM_ENULL;
-        if (!aligned16(wq[e])) return QMM_EALIGN;
-    }
-    if (!aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(ids) & 3u)) return QMM_EALIGN;
-    unsigned int *status = status_ptr();
-    if (!status) return QMM_ECUDA;
-    const bool xbf16 = (qtype & QMM_X_BF16) != 0, per_slot = (qtype & QMM_X_PER_SLOT) != 0;
-    const int rc = launch_gemv_tc_id(qt, xbf16, wq, E, N, K, x, per_slot, ids, M, topk, y, status,
-                                     static_cast<cudaStream_t>(stream));
-    if (rc != -3) return rc;
-    return launch_mvid(qt, xbf16, wq, E, N, K, x, per_slot, ids, M, topk, y, status,
-                       static_cast<cudaStream_t>(stream));
+    if (E < 1 || M < 1 || topk < 1) return QMM_ERANGE;
+    return pick_id_path(qt, E, K, M, topk);
 }
 
 int qmm_dequant(const void *wq, int qtype, int64_t N, int64_t K, float *w_out, void *stream) {

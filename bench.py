@@ -4,7 +4,10 @@ A step is one pass of the whole hot path over the workload the pages time (candl
 64-token tile for the quantized matrix-matrix kernel", section "This branch, kernel level"): the seven
 projections of one Qwen3-Embedding-4B layer (attn_q/k/v/output Q4_K/Q6_K, ffn_gate/up Q4_K, ffn_down Q6_K)
 at every token count M in {1, 2, 7, 32, 33, 64, 96, 100, 128, 130, 136, 512, 2048}, plus the 65-token case
-as a batch of two sequences: 105 qmm calls. M <= 16 runs the mat-vec path, larger M the tcgen05 path.
+as a batch of two sequences: 105 projections. M <= 16 runs the mat-vec path, larger M the tcgen05 path. At
+M <= 16 the projections that share an input and a type go in one qmm_batch launch (attn_q + attn_k,
+ffn_gate + ffn_up), as a model chains them; the `unbatched` object times every projection as its own call.
+All calls pass QMM_W_STATIC (the weights are model data that no kernel of the step writes).
 
 Metric: weight-GB/s of the M <= 16 calls against HBM (value), and TFLOPS of the M >= 64 calls against the
 bf16 tensor-core peak (tflops_m_ge_64). Inputs are resident in HBM; weights rotate through 7 copies of the
@@ -78,6 +81,13 @@ def load_peaks():
         return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
                 "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# Projections that take the same input and share a type: at M <= 16 a step serves each pair with one
+# qmm_batch launch, as a model chains them (the query and key projections of the attention input; the gate
+# and up projections of the feed-forward input). attn_v shares the input but not the type (Q6_K).
+SHARED_INPUT = {"attn_q": "attn_k", "ffn_gate": "ffn_up"}
+SHARED_PARTNERS = set(SHARED_INPUT.values())
 
 
 def bench_config(world):
@@ -233,13 +243,14 @@ def run_ours(args):
             qmm.qmm_quantize(w32, qt, N, K, buf)
             wq[(copy, name)] = buf
             del w32
-    xs, ys = {}, {}
+    xs, ys, ys2 = {}, {}, {}
     ws_bytes = 0
     for name, N, K, qt, M, b in calls:
         if (M, K, b) not in xs:
             xs[(M, K, b)] = torch.from_numpy(synthetic.activations(M, K, seed=M + 17 * b)).to(dev)
         if (M, N) not in ys:
             ys[(M, N)] = torch.empty((M, N), dtype=torch.float32, device=dev)
+            ys2[(M, N)] = torch.empty((M, N), dtype=torch.float32, device=dev)   # a batch partner's output
         ws_bytes = max(ws_bytes, qmm.qmm_workspace_size(qt, N, K, M))
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
@@ -250,7 +261,8 @@ def run_ours(args):
     P = ctypes.c_void_p
 
     ncalls = len(calls)
-    per_step_launches = sum(qmm.qmm_launch_count(c[3], c[1], c[2], c[4]) for c in calls)
+    per_step_launches = sum(qmm.qmm_launch_count(c[3], c[1], c[2], c[4]) for c in calls
+                            if not (c[4] <= 16 and c[0] in SHARED_PARTNERS))
 
     # One CUDA graph per (weight copy, token-count group): the group's calls are captured back to back, so
     # consecutive kernels overlap through programmatic dependent launch; events sit only between groups.
@@ -262,10 +274,23 @@ def run_ours(args):
         groups[-1][1].append(i)
 
     def run_group(copy, idxs):
+        done = set()
         for i in idxs:
+            if i in done:
+                continue
             name, N, K, qt, M, b = calls[i]
-            rc = L.qmm_ws(P(wq[(copy, name)].data_ptr()), qmm.TYPE_ID[qt], N, K, P(xs[(M, K, b)].data_ptr()), M,
-                          P(ys[(M, N)].data_ptr()), P(ws.data_ptr()), ws.numel(), P(stream.cuda_stream))
+            partner = SHARED_INPUT.get(name)
+            if M <= 16 and partner is not None:
+                # the projections that share this input and type: one mat-vec launch (qmm_batch)
+                j = next(j for j in idxs if calls[j][0] == partner and calls[j][5] == b)
+                done.add(j)
+                N2 = calls[j][1]
+                qmm.qmm_batch([wq[(copy, name)], wq[(copy, partner)]], qmm.TYPE_ID[qt] | qmm.W_STATIC, [N, N2], K,
+                              xs[(M, K, b)], [ys[(M, N)], ys2[(M, N2)]])
+                continue
+            rc = L.qmm_ws(P(wq[(copy, name)].data_ptr()), qmm.TYPE_ID[qt] | qmm.W_STATIC, N, K,
+                          P(xs[(M, K, b)].data_ptr()), M, P(ys[(M, N)].data_ptr()), P(ws.data_ptr()), ws.numel(),
+                          P(stream.cuda_stream))
             if rc:
                 raise RuntimeError("qmm_ws: " + qmm.qmm_strerror(rc))
 
@@ -378,6 +403,7 @@ def run_ours(args):
             print("M=%-6s %2d calls %9.2f us %8.1f GB/s %8.2f TFLOP/s" % (
                 label, len(idxs), group_ms[gi] * 1e3, wb / (group_ms[gi] * 1e-3) / 1e9,
                 fl / (group_ms[gi] * 1e-3) / 1e12), file=sys.stderr)
+    unbatched = run_unbatched(args, qmm, torch, dev, wq, peaks) if not args.case else None
     e2e = run_e2e(args, qmm, torch, dev, calls, wq, ws) if not args.case else None
     del wq, xs, ys, graphs
     torch.cuda.empty_cache()
@@ -401,7 +427,7 @@ def run_ours(args):
             "config": bench_config(world) if not args.case else {"workload": "single call " + args.case},
             "roofline": roof, "roofline_classes": cls_out, "roofline_step": step_summary,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": per_step_launches * args.steps,
-            "clocks": clocks, "per_m": per_m, "small_q4_0": small_q4_0, "qwen3_06b": qwen3_06b, "moe": moe,
+            "clocks": clocks, "per_m": per_m, "unbatched": unbatched, "small_q4_0": small_q4_0, "qwen3_06b": qwen3_06b, "moe": moe,
             "sweep": sweep, "peaks": peaks,
         }
         print(json.dumps(line))
@@ -462,6 +488,9 @@ def aggregate(cases, key_w="wbytes"):
     return round(r / t, 4) if t else None
 
 
+PREFILL_TOKENS = [32, 64, 128, 256]
+
+
 def run_moe(args, qmm, torch, dev, peaks):
     """The expert-indexed product on the MoE workload: 128 experts of 4096 x K Q4_0 (K in {512, 768, 1024}),
     top-8 routing, n tokens in {1, 2, 4, 8, 12, 16, 24}. Calls rotate through 64 id tables (8 distinct experts
@@ -473,7 +502,7 @@ def run_moe(args, qmm, torch, dev, peaks):
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
     stream = torch.cuda.Stream()
-    out, tot_b, tot_t, tot_r = [], 0.0, 0.0, 0.0
+    out, prefill, tot_b, tot_t, tot_r = [], [], 0.0, 0.0, 0.0
     for K in synthetic.MOE_K:
         rb = qmm.row_bytes("Q4_0", K)
         banks = []
@@ -502,12 +531,48 @@ def run_moe(args, qmm, torch, dev, peaks):
             tot_b += wbytes
             tot_t += us
             tot_r += roof
+        # prefill-sized routing, beyond the verify batches: the mat-vec expert kernel (path 1) beside the
+        # tensor-core expert kernel (path 2) on the same calls
+        for n in PREFILL_TOKENS:
+            tabs = [synthetic.expert_ids(n, batch=b) for b in range(8)]
+            idss = [torch.from_numpy(t).to(dev) for t in tabs]
+            distinct = float(np.mean([len(np.unique(t)) for t in tabs]))
+            x = torch.randn(n, K, device=dev, generator=gen)
+            y = torch.empty(n, TOPK, N, device=dev)
+            row = {"K": K, "n": n, "auto_path": qmm.qmm_id_pick_path("Q4_0", E, K, n, TOPK)}
+            wbytes = distinct * rb * N
+            t_roof = max((wbytes + n * K * 4) / (peaks["hbm_gbs"] * 1e9) * 1e6,
+                         2.0 * n * TOPK * N * K / (peaks["bf16_tflops"] * 1e12) * 1e6)
+            for path in (1, 2):
+                fns = [(lambda i=i, path=path: qmm.qmm_id(banks[i % NBANK], "Q4_0", N, K, x, idss[i % 8], y,
+                                                          path=path)) for i in range(16)]
+                us = time_graph(torch, stream, fns)
+                row["us_path%d" % path] = round(us, 2)
+                row["tflops_path%d" % path] = round(2.0 * n * TOPK * N * K / us / 1e6, 2)
+                row["frac_path%d" % path] = round(t_roof / us, 4)
+            prefill.append(row)
+        # dense routing: the same tokens routed within the first 16 experts (32-256 pairs per expert)
+        for n in (64, 256, 512):
+            tabs = [synthetic.expert_ids(n, E=16, topk=TOPK, batch=b) for b in range(8)]
+            idss = [torch.from_numpy(t).to(dev) for t in tabs]
+            x = torch.randn(n, K, device=dev, generator=gen)
+            y = torch.empty(n, TOPK, N, device=dev)
+            row = {"K": K, "n": n, "experts": 16, "auto_path": qmm.qmm_id_pick_path("Q4_0", E, K, n, TOPK)}
+            for path in (1, 2):
+                fns = [(lambda i=i, path=path: qmm.qmm_id(banks[i % NBANK], "Q4_0", N, K, x, idss[i % 8], y,
+                                                          path=path)) for i in range(16)]
+                us = time_graph(torch, stream, fns)
+                row["us_path%d" % path] = round(us, 2)
+                row["tflops_path%d" % path] = round(2.0 * n * TOPK * N * K / us / 1e6, 2)
+            prefill.append(row)
         del banks
         torch.cuda.empty_cache()
     return {"metric": "expert-indexed weight-GB/s (distinct experts' bytes / time)", "unit": "GB/s",
             "value": round(tot_b / tot_t / 1e3, 1), "frac": round(tot_r / tot_t, 4),
             "workload": "2 banks x 128 experts x 4096 x K Q4_0, top-8, K in {512,768,1024}, n in "
-                        "{1,2,4,8,12,16,24}; 64 id tables rotating", "cases": out}
+                        "{1,2,4,8,12,16,24}; 64 id tables rotating", "cases": out,
+            "prefill": {"tokens": PREFILL_TOKENS, "note": "mat-vec expert kernel (path 1) beside the tensor-core "
+                        "expert kernel (path 2); auto_path is qmm_id's choice", "cases": prefill}}
 
 
 def run_small_q4_0(qmm, torch, dev, peaks):
@@ -597,6 +662,31 @@ def run_sweep(qmm, torch, dev, peaks):
             "frac": aggregate(allc), "types": out}
 
 
+def run_unbatched(args, qmm, torch, dev, wq, peaks):
+    """The layer's M <= 16 calls as seven separate qmm_ws calls (no projection batched), for comparison with
+    the step's batched form. One CUDA graph per (weight copy, token count)."""
+    stream = torch.cuda.Stream()
+    out, tot_b, tot_t, tot_r = [], 0.0, 0.0, 0.0
+    for M in (1, 2, 7):
+        xs = {K: torch.from_numpy(synthetic.activations(M, K, seed=M)).to(dev) for K in {l[2] for l in LAYER}}
+        ys = {name: torch.empty((M, N), dtype=torch.float32, device=dev) for name, N, K, qt in LAYER}
+
+        def step(copy):
+            for name, N, K, qt in LAYER:
+                qmm.qmm_ws(wq[(copy, name)], qmm.TYPE_ID[qt] | qmm.W_STATIC, N, K, xs[K], ys[name], None)
+
+        fns = [(lambda c=c: step(c)) for c in range(COPIES)]
+        us = time_graph(torch, stream, fns, replays=max(4, args.steps // COPIES))
+        wb = sum(weight_bytes(N, K, qt) for _, N, K, qt in LAYER)
+        roof = sum(call_roofline(M, N, K, weight_bytes(N, K, qt), 4, peaks)[0] for _, N, K, qt in LAYER)
+        out.append({"M": M, "us": round(us, 2), "weight_gbs": round(wb / us / 1e3, 1), "frac": round(roof / us, 4)})
+        tot_b += wb
+        tot_t += us
+        tot_r += roof
+    return {"metric": "weight-GB/s of the M<=16 calls, every projection its own call", "unit": "GB/s",
+            "value": round(tot_b / tot_t / 1e3, 1), "frac": round(tot_r / tot_t, 4), "per_m": out}
+
+
 def run_e2e(args, qmm, torch, dev, calls, wq, ws):
     """The headline metric end to end through the public API with host buffers: every step copies the
     activations of its M <= 16 calls from pinned host memory to the device (one copy of all of them), runs
@@ -622,10 +712,20 @@ def run_e2e(args, qmm, torch, dev, calls, wq, ws):
 
     def step(copy):
         dx.copy_(hx, non_blocking=True)
+        views = {}
         for i, (name, N, K, qt, M, b) in enumerate(small):
-            x = dx[xoff[(M, K)]:xoff[(M, K)] + M * K].view(M, K)
-            y = dy[yoff[i]:yoff[i] + M * N].view(M, N)
-            qmm.qmm_ws(wq[(copy, name)], qt, N, K, x, y, ws)
+            views[(name, M)] = (dx[xoff[(M, K)]:xoff[(M, K)] + M * K].view(M, K), dy[yoff[i]:yoff[i] + M * N].view(M, N))
+        for name, N, K, qt, M, b in small:
+            if name in SHARED_PARTNERS:
+                continue
+            x, y = views[(name, M)]
+            partner = SHARED_INPUT.get(name)
+            if partner:
+                N2 = next(c[1] for c in small if c[0] == partner)
+                qmm.qmm_batch([wq[(copy, name)], wq[(copy, partner)]], qmm.TYPE_ID[qt] | qmm.W_STATIC, [N, N2], K, x,
+                              [y, views[(partner, M)][1]])
+            else:
+                qmm.qmm_ws(wq[(copy, name)], qmm.TYPE_ID[qt] | qmm.W_STATIC, N, K, x, y, ws)
         hy.copy_(dy, non_blocking=True)
 
     stream = torch.cuda.Stream()
@@ -654,8 +754,9 @@ def run_e2e(args, qmm, torch, dev, calls, wq, ws):
     wb = sum(weight_bytes(c[1], c[2], c[3]) for c in small)
     return {"value": round(wb / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": nx * 4, "d2h_bytes_per_step": ny * 4, "steps": steps,
-            "calls": "the 21 calls with M<=16, one host-to-device copy of their activations and one "
-                     "device-to-host copy of their results per step, replayed as CUDA graphs"}
+            "calls": "the 21 projections with M<=16 (q+k and gate+up batched as in the step), one host-to-device "
+                     "copy of their activations and one device-to-host copy of their results per step, replayed "
+                     "as CUDA graphs"}
 
 
 # ---------------------------------------------------------------------------------------- oracle legs

@@ -50,7 +50,8 @@ A = 0x1000  # a 16-byte aligned fake address; never dereferenced: every call bel
 
 @pytest.mark.parametrize("args,code", [
     ((P(A), 14, 64, 64, P(A), 1, P(A), None), -1),           # bad type
-    ((P(A), 0x203, 64, 64, P(A), 1, P(A), None), -1),        # unknown flag bit
+    ((P(A), 0x203, 64, 64, P(A), 1, P(A), None), -1),        # not a flag of qmm (per-slot x is qmm_id's)
+    ((P(A), 0x803, 64, 64, P(A), 1, P(A), None), -1),        # unknown flag bit
     ((P(A), 3, 64, 48, P(A), 1, P(A), None), -2),            # K not a multiple of 32 for Q4_0
     ((P(A), 10, 64, 512 + 32, P(A), 1, P(A), None), -2),     # K not a multiple of 256 for Q4_K
     ((P(A), 3, 0, 64, P(A), 1, P(A), None), -3),             # N = 0
@@ -83,7 +84,7 @@ def test_qmm_id_errors(L):
 def test_qmm_id_flags(L):
     ptrs = (ctypes.c_void_p * 2)(A, A)
     arr = ctypes.cast(ptrs, P)
-    assert L.qmm_id(arr, 2, 3 | 0x400, 64, 64, P(A), P(A), 1, 8, P(A), None) == -1   # unknown flag
+    assert L.qmm_id(arr, 2, 3 | 0x800, 64, 64, P(A), P(A), 1, 8, P(A), None) == -1   # unknown flag
     assert L.qmm_id(arr, 2, 3 | 0x200, 64, 48, P(A), P(A), 1, 8, P(A), None) == -2   # per-slot x accepted
     assert L.qmm(P(A), 3 | 0x200, 64, 64, P(A), 1, P(A), None) == -1                # not a qmm flag
 
@@ -142,8 +143,9 @@ def test_noalloc_checks_arguments_first(L):
 def test_qmm_id_path_choice(L):
     # a few pairs per expert: the mat-vec expert kernel; many (prefill): the tensor-core one
     assert qmm.qmm_id_pick_path("Q4_0", 128, 512, 24, 8) == 1
-    assert qmm.qmm_id_pick_path("Q4_0", 128, 512, 256, 8) == 2
-    assert qmm.qmm_id_pick_path("F32", 8, 256, 64, 2) == 2
+    assert qmm.qmm_id_pick_path("Q4_0", 128, 512, 256, 8) == 1
+    assert qmm.qmm_id_pick_path("Q4_0", 16, 512, 256, 8) == 2
+    assert qmm.qmm_id_pick_path("F32", 2, 256, 64, 2) == 2
     ptrs = (ctypes.c_void_p * 2)(A, A)
     arr = ctypes.cast(ptrs, P)
     assert L.qmm_id_with_path(arr, 2, 3, 64, 64, P(A), P(A), 1, 8, P(A), 3, None) == -7   # no such path

@@ -166,3 +166,22 @@ def test_tile_invariance(qtype):
                 d = bit_differences(o, outs[0])
                 assert d == 0, "%s %dx%dx%dx%d: %d of %d outputs differ between tiles 32 and %d" % (
                     qtype, batch, M, N, K, d, o.size, t)
+
+
+@pytest.mark.parametrize("qtype", ["Q4_K", "Q6_K", "Q4_0"])
+@pytest.mark.parametrize("M", [1, 7, 40, 300])
+def test_static_weights_flag_same_bits(qtype, M):
+    """QMM_W_STATIC only moves the weight reads before the wait for the preceding kernel: same bits."""
+    torch = torch_cuda()
+    N, K = 260, 1024
+    wq, x = _case(qtype, N, K, M, seed=M + 11)
+    a = _run(qmm.qmm, wq, qtype, N, K, x)
+    b = _run(qmm.qmm, wq, qmm.TYPE_ID[qtype] | qmm.W_STATIC, N, K, x)
+    assert bit_differences(a, b) == 0
+    nb = qmm.qmm_workspace_size(qtype, N, K, M)
+    ws = torch.empty(max(nb, 1), dtype=torch.uint8, device="cuda")
+    c = _run(qmm.qmm_ws, wq, qtype, N, K, x, workspace=ws)
+    d = _run(qmm.qmm_ws, wq, qmm.TYPE_ID[qtype] | qmm.W_STATIC, N, K, x, workspace=ws)
+    assert bit_differences(c, d) == 0
+    ref, bnd = oracle.qmm(qtype, wq, N, K, x)
+    check_tol(b, ref, bnd, TOL_FP32 if M <= 16 else TOL_BF16, "%s M=%d" % (qtype, M))

@@ -142,7 +142,7 @@ def test_qmm_id_tensor_core_128_experts(n):
     check_tol(y2, ref, bnd, TOL_BF16, "tensor-core n=%d" % n)
     y1 = _run_path(wqs, "Q4_0", N, K, x, ids, 1)
     check_tol(y1, ref, bnd, TOL_FP32, "mat-vec n=%d" % n)
-    assert qmm.qmm_id_pick_path("Q4_0", E, K, n, topk) == (2 if n * topk >= 16 * min(E, n * topk) else 1)
+    assert qmm.qmm_id_pick_path("Q4_0", E, K, n, topk) == (2 if n * topk >= 48 * min(E, n * topk) else 1)
 
 
 @pytest.mark.parametrize("qtype", ["Q4_K", "Q6_K", "Q8_0", "A4G64", "Q5_1", "F16", "F32"])

@@ -11,7 +11,7 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["QmmError", "TYPES", "TYPE_ID", "X_BF16", "X_PER_SLOT", "build", "lib", "qmm", "qmm_ws", "qmm_workspace_size",
+__all__ = ["QmmError", "TYPES", "TYPE_ID", "X_BF16", "X_PER_SLOT", "W_STATIC", "build", "lib", "qmm", "qmm_ws", "qmm_batch", "qmm_workspace_size",
            "qmm_launch_count", "qmm_plan_info", "qmm_noalloc", "NOALLOC_SCRATCH_BYTES",
            "qmm_id", "qmm_id_with_path", "qmm_id_pick_path", "qmm_with_tile", "qmm_pick_tile", "qmm_pick_path", "qmm_dequant", "qmm_quantize",
            "qmm_type_info", "qmm_get_status", "qmm_debug_stall", "qmm_strerror", "row_bytes", "EXPORTS"]
@@ -24,10 +24,11 @@ TYPES = ["F32", "F16", "BF16", "Q4_0", "Q4_1", "Q5_0", "Q5_1", "Q8_0",
 TYPE_ID = {n: i for i, n in enumerate(TYPES)}
 X_BF16 = 0x100
 X_PER_SLOT = 0x200
+W_STATIC = 0x400      # the kernel launched just before the call does not write the weights
 STATUS_BAD_ID, STATUS_TIMEOUT = 0x1, 0x2
 
 # Every symbol include/qmm.h declares.
-EXPORTS = ["qmm", "qmm_ws", "qmm_workspace_size", "qmm_noalloc", "qmm_id", "qmm_id_with_path", "qmm_id_pick_path",
+EXPORTS = ["qmm", "qmm_ws", "qmm_workspace_size", "qmm_noalloc", "qmm_batch", "qmm_id", "qmm_id_with_path", "qmm_id_pick_path",
            "qmm_with_tile", "qmm_pick_tile",
            "qmm_pick_path", "qmm_launch_count", "qmm_plan_info", "qmm_dequant", "qmm_quantize", "qmm_type_info", "qmm_get_status",
            "qmm_debug_stall", "qmm_strerror"]
@@ -60,6 +61,7 @@ def lib():
             "qmm": ([P, I, I64, I64, P, I64, P, P], I),
             "qmm_ws": ([P, I, I64, I64, P, I64, P, P, SZ, P], I),
             "qmm_noalloc": ([P, I, I64, I64, P, I64, P, P], I),
+            "qmm_batch": ([I, P, P, P, I, I64, P, I64, P], I),
             "qmm_workspace_size": ([I, I64, I64, I64], SZ),
             "qmm_id": ([P, I64, I, I64, I64, P, P, I64, I, P, P], I),
             "qmm_id_with_path": ([P, I64, I, I64, I64, P, P, I64, I, P, I, P], I),
@@ -169,6 +171,21 @@ def qmm_ws(wq, qtype, N: int, K: int, x, y, workspace, stream=None):
                       _ptr(workspace), nbytes, _stream(stream))
     _check(rc, "qmm_ws")
     return y
+
+
+def qmm_batch(wqs, qtype, Ns, K: int, x, ys, stream=None):
+    """ys[i][M, N_i] = x[M, K] @ dequant(wqs[i])^T for matrices of one type that share x (one mat-vec launch
+    for all of them when M <= 16)."""
+    M = x.shape[0]
+    n = len(wqs)
+    W = (ctypes.c_void_p * n)(*[w.data_ptr() for w in wqs])
+    NN = (ctypes.c_int64 * n)(*[int(v) for v in Ns])
+    Y = (ctypes.c_void_p * n)(*[y.data_ptr() for y in ys])
+    rc = lib().qmm_batch(n, ctypes.cast(W, ctypes.c_void_p), ctypes.cast(NN, ctypes.c_void_p),
+                         ctypes.cast(Y, ctypes.c_void_p), _qt(qtype) | _xflag(x), int(K), _ptr(x), int(M),
+                         _stream(stream))
+    _check(rc, "qmm_batch")
+    return ys
 
 
 def qmm_noalloc(wq, qtype, N: int, K: int, x, y, stream=None):

@@ -285,27 +285,14 @@ struct QuantizeLaunch {
 };
 }  // namespace
 
-namespace deq {
-// An empty kernel launched (without programmatic dependent launch) after a kernel that writes a matrix the
-// matmul kernels may read as weights. Those kernels read their weights before waiting for their predecessor
-// in the stream; this launch starts only once the writer has completed, so it is a safe predecessor.
-__global__ void ordering_kernel() {}
-}  // namespace deq
-
-static int ordered(int rc, cudaStream_t st) {
-    if (rc) return rc;
-    deq::ordering_kernel<<<1, 32, 0, st>>>();
-    return cudaGetLastError() == cudaSuccess ? 0 : -6;
-}
-
 int launch_dequant(int qt, const void *wq, int64_t N, int64_t K, float *out, cudaStream_t st) {
     DequantLaunch f{wq, N, K, out, st};
-    return ordered(dispatch_type(qt, f), st);
+    return dispatch_type(qt, f);
 }
 
 int launch_quantize(int qt, const float *w, int64_t N, int64_t K, void *out, cudaStream_t st) {
     QuantizeLaunch f{w, N, K, out, st};
-    return ordered(dispatch_type(qt, f), st);
+    return dispatch_type(qt, f);
 }
 
 }  // namespace wqk

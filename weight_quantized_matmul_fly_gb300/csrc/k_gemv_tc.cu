@@ -516,10 +516,22 @@ __device__ __forceinline__ void macro_step(const typename Frag<QT>::Raw &cur0, c
 //     it waits on a stage's mbarrier, decodes the stage and refills it with the macro block `ns` steps
 //     ahead. Used when the tile does not fit.
 // Few large copies stream faster than many small ones, which is why the resident mode is preferred.
+// Several weight matrices of one type and one K that take the same activations, served by one launch: the
+// CTAs cover the row blocks of matrix 0, then of matrix 1, ...; rb0[i] is the first CTA (x index) of matrix i.
+constexpr int kMaxMulti = 8;
+struct Multi {
+    int count;                      // 0: a single matrix (the kernel's own wq, N, y)
+    int rb0[kMaxMulti + 1];
+    const uint8_t *wq[kMaxMulti];
+    int N[kMaxMulti];
+    float *y[kMaxMulti];
+};
+
 template <int QT, int NT, bool XBF16, int KW>
 __global__ void __launch_bounds__(256, 2)
-    gemv_tc_kernel(const uint8_t *__restrict__ wq, int N, int64_t K, int64_t rowbytes, const void *__restrict__ x,
-                   int M, float *__restrict__ y, int kseg, int ns, unsigned int *__restrict__ status, int stall) {
+    gemv_tc_kernel(const uint8_t *__restrict__ wq_, int N_, int64_t K, int64_t rowbytes, const void *__restrict__ x,
+                   int M, float *__restrict__ y_, int kseg, int ns, unsigned int *__restrict__ status, int stall,
+                   int early, const __grid_constant__ Multi multi) {
     using F = Frag<QT>;
     using LY = Layout<NT, XBF16>;
     constexpr int WARPS = LY::WARPS, RG = WARPS / KW;
@@ -544,10 +556,24 @@ __global__ void __launch_bounds__(256, 2)
     float *sx = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(xs) + (size_t)scols * xst * 2);
     float *part = sx + (size_t)TOK * sxs;             // [WARPS][16][TOK]
 
+    // this CTA's matrix and its row block within it
+    const uint8_t *wq = wq_;
+    int N = N_;
+    float *y = y_;
+    int bx = blockIdx.x;
+    if (multi.count > 0) {
+        int i = 0;
+        while (i + 1 < multi.count && bx >= multi.rb0[i + 1]) ++i;
+        bx -= multi.rb0[i];
+        wq = multi.wq[i];
+        N = multi.N[i];
+        y = multi.y[i];
+    }
+
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
     const int rg = warp / KW, ks = warp % KW;
-    const int nrow0 = blockIdx.x * (16 * RG) + 16 * rg;
+    const int nrow0 = bx * (16 * RG) + 16 * rg;
     // this warp's macro blocks: a balanced share of the segment's
     const int64_t smb = kb / 256, nmb = (ke - kb + 255) / 256;
     const int64_t mb_beg = smb + (nmb * ks) / KW, mb_end = smb + (nmb * (ks + 1)) / KW;
@@ -596,20 +622,36 @@ __global__ void __launch_bounds__(256, 2)
     const bool stall_here = stall != 0 && blockIdx.x == 0 && blockIdx.y == 0;
     if (stall_here && warp == 0 && lane == 0) ptx::mbar_init(never, 1);   // visible after the staging barrier
 
-    // The weights are requested before waiting for the preceding kernel in the stream (they are model data
-    // that no kernel of this library writes); activations and outputs are touched only after.
+    // Before waiting for the preceding kernel in the stream, the weights this warp will copy are only
+    // prefetched into L2 (coherent, so never stale even if that kernel wrote them); they are copied into
+    // shared memory, and activations and outputs touched, only after the wait. With `early` (the caller
+    // states that the preceding kernel does not write the weights) the copies themselves are issued before
+    // the wait, so that they overlap the end of the preceding kernel.
     if (lane == 0)
         for (int i = 0; i < ns; ++i) ptx::mbar_init(&wbar[i], 16);
+    if (resident && ks == 0 && lane == 0) ptx::mbar_init(gbar, 16);
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
     __syncwarp();
-    if (resident) {
-        // one copy per row: the segment's blocks of that row (warps with ks > 0 only wait for them)
-        if (ks == 0) {
-            if (lane == 0) ptx::mbar_init(gbar, 16);
-            ptx::fence_mbar_init();
-            __syncwarp();
-            if (lane < 16) {
+    if (!early && lane < 16 && (!resident || ks == 0) && nsteps + (resident ? 1 : 0) > 0) {
+        // resident: the row's whole segment; ring: this warp's macro blocks of the row
+        const int64_t pb = resident ? smb : mb_beg;
+        const int64_t pe_blocks = resident ? ((nblocks_row - smb * BPM) < (int64_t)(kseg / QK) ? nblocks_row - smb * BPM
+                                                                                              : (int64_t)(kseg / QK))
+                                           : (mb_end - mb_beg) * BPM;
+        const uintptr_t a = reinterpret_cast<uintptr_t>(wq + (int64_t)crow * rowbytes + pb * BPM * BYTES);
+        uintptr_t e = a + (uintptr_t)pe_blocks * BYTES;
+        const uintptr_t rend = reinterpret_cast<uintptr_t>(wq + (int64_t)(crow + 1) * rowbytes);
+        if (e > rend) e = rend;
+        const uintptr_t a0 = a & ~(uintptr_t)15;
+        uintptr_t e1 = (e + 15) & ~(uintptr_t)15;
+        if (e1 > wend) e1 = wend & ~(uintptr_t)15;
+        if (e1 > a0) ptx::prefetch_l2(reinterpret_cast<const void *>(a0), (uint32_t)(e1 - a0));
+    }
+    auto copy_weights = [&]() {
+        if (resident) {
+            // one copy per row: the segment's blocks of that row (warps with ks > 0 only wait for them)
+            if (ks == 0 && lane < 16) {
                 const uintptr_t a = reinterpret_cast<uintptr_t>(wq + (int64_t)crow * rowbytes + smb * BPM * BYTES);
                 const int64_t sblocks = (nblocks_row - smb * BPM) < (int64_t)(kseg / QK) ? nblocks_row - smb * BPM
                                                                                          : (int64_t)(kseg / QK);
@@ -622,14 +664,16 @@ __global__ void __launch_bounds__(256, 2)
                 ptx::mbar_arrive_expect_tx(gbar, e1 > a0 ? (uint32_t)(e1 - a0) : 0u);
                 if (e1 > a0) ptx::bulk_load(dst, reinterpret_cast<const void *>(a0), (uint32_t)(e1 - a0), gbar);
             }
+        } else {
+            const int npre = nsteps < ns ? nsteps : ns;
+            for (int i = 0; i < npre; ++i) issue(i);
         }
-    } else {
-        const int npre = nsteps < ns ? nsteps : ns;
-        for (int i = 0; i < npre; ++i) issue(i);
-    }
+    };
+    if (early) copy_weights();
     if (gridDim.y > 1) cluster_arrive_relaxed();      // matched by the wait before the partials move
     asm volatile("griddepcontrol.launch_dependents;");
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!early) copy_weights();
 
     // ---- stage this segment's activations (tokens < M): bf16 columns and per-unit sums. The loads of XU
     //      iterations are issued together so that their latencies overlap.
@@ -782,7 +826,7 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
         for (int q = 0; q < KW; ++q) sum += part[((size_t)(rgi * KW + q) * 16 + rr) * TOK + tk];
         if (S == 1) {
-            const int n = blockIdx.x * (16 * RG) + r;
+            const int n = bx * (16 * RG) + r;
             if (n < N) y[(int64_t)tk * N + n] = sum;
         } else {
             st_dsmem_f32(red0 + 4u * (rank * (uint32_t)nres + (uint32_t)idx), sum);
@@ -795,7 +839,7 @@ __global__ void __launch_bounds__(256, 2)
                 const int r = idx / mtok, tk = idx - r * mtok;
                 float sum = 0.0f;
                 for (int q = 0; q < S; ++q) sum += red[q * nres + idx];
-                const int n = blockIdx.x * (16 * RG) + r;
+                const int n = bx * (16 * RG) + r;
                 if (n < N) y[(int64_t)tk * N + n] = sum;
             }
         }
@@ -1138,14 +1182,25 @@ int64_t gtc_capacity(int64_t S, size_t smem) {
 }
 
 template <int QT, int NT, bool XBF16, int KW>
-int launch_gtc_kw(const void *wq, int64_t N, int64_t K, const void *x, int M, float *y, int64_t S, int64_t kseg,
-                  int ns, unsigned int *status, cudaStream_t st, int stall) {
+int launch_gtc_kw(const MatSet &ms, int64_t K, const void *x, int M, int64_t S, int64_t kseg, int ns,
+                  unsigned int *status, cudaStream_t st, int stall, int early) {
     using LY = gtc::Layout<NT, XBF16>;
     constexpr int UNIT = gtc::Frag<QT>::UNIT, RG = LY::WARPS / KW;
     auto kern = gtc::gemv_tc_kernel<QT, NT, XBF16, KW>;
     if (gtc_capacity<QT, NT, XBF16, KW>(1, 0) <= 0) return -6;   // also sets the kernel's attributes
+    gtc::Multi multi = {};
+    int64_t nrb = 0;
+    for (int i = 0; i < ms.count; ++i) {
+        multi.rb0[i] = (int)nrb;
+        multi.wq[i] = static_cast<const uint8_t *>(ms.wq[i]);
+        multi.N[i] = (int)ms.N[i];
+        multi.y[i] = ms.y[i];
+        nrb += (ms.N[i] + 16 * RG - 1) / (16 * RG);
+    }
+    multi.rb0[ms.count] = (int)nrb;
+    multi.count = ms.count > 1 ? ms.count : 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((N + 16 * RG - 1) / (16 * RG)), (unsigned)S, 1);
+    cfg.gridDim = dim3((unsigned)nrb, (unsigned)S, 1);
     cfg.blockDim = dim3(LY::WARPS * 32, 1, 1);
     constexpr int MB_BYTES = 256 / TypeInfo<QT>::QK * TypeInfo<QT>::BYTES;
     cfg.dynamicSmemBytes = (ns == 0 ? LY::BARS + LY::tile_bytes(RG, (int)(kseg / 256 * MB_BYTES)) +
@@ -1162,8 +1217,9 @@ int launch_gtc_kw(const void *wq, int64_t N, int64_t K, const void *x, int M, fl
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t *>(wq), (int)N, K, row_bytes(QT, K), x,
-                                       M, y, (int)kseg, ns, status, stall);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, multi.count ? multi.wq[0] : static_cast<const uint8_t *>(ms.wq[0]),
+                                       (int)ms.N[0], K, row_bytes(QT, K), x, M, ms.y[0], (int)kseg, ns, status, stall,
+                                       early, multi);
     return e == cudaSuccess ? 0 : -6;
 }
 
@@ -1175,12 +1231,19 @@ int launch_gtc_kw(const void *wq, int64_t N, int64_t K, const void *x, int M, fl
 // more row groups per CTA so that the activations each CTA stages stay small next to its weights. Each
 // warp's ring takes as many stages as the shared memory left over allows (at most its macro blocks).
 template <int QT, int NT, bool XBF16>
-int launch_gtc_t(const void *wq, int64_t N, int64_t K, const void *x, int M, float *y, unsigned int *status,
-                 cudaStream_t st, bool dry, int stall) {
+int launch_gtc_t(const MatSet &ms, int64_t K, const void *x, int M, unsigned int *status, cudaStream_t st, bool dry,
+                 int stall, int early) {
     using LY = gtc::Layout<NT, XBF16>;
     constexpr int UNIT = gtc::Frag<QT>::UNIT, SLOT = gtc::slot_bytes<QT>();
     constexpr int MB_BYTES = 256 / TypeInfo<QT>::QK * TypeInfo<QT>::BYTES;   // bytes of a macro block
-    const int64_t ngroups = (N + 15) / 16;
+    int64_t total_rows = 0;
+    for (int i = 0; i < ms.count; ++i) total_rows += ms.N[i];
+    // CTAs in x for `rg` row groups per CTA: every matrix's row blocks separately
+    auto row_blocks = [&](int64_t rg) {
+        int64_t n = 0;
+        for (int i = 0; i < ms.count; ++i) n += ((ms.N[i] + 15) / 16 + rg - 1) / rg;
+        return n;
+    };
     const int64_t nmacro = (K + 255) / 256;
     // K slices per CTA: more for fewer tokens (the staged activations are then small); only the counts
     // that some M of this column-group count can use are compiled.
@@ -1190,7 +1253,7 @@ int launch_gtc_t(const void *wq, int64_t N, int64_t K, const void *x, int M, flo
     int best_kw = 1, best_s = 1, best_ns = 1;
     int64_t best_cost = -1, best_ctas = 0;
     for (int kw = 1; kw <= kw_cap; kw *= 2) {
-        const int64_t nrb = (ngroups + (8 / kw) - 1) / (8 / kw);
+        const int64_t nrb = row_blocks(8 / kw);
         for (int64_t S = 1; S <= 8 && S <= nmacro; ++S) {
             const int64_t kseg = ((nmacro + S - 1) / S) * 256;
             if ((K + kseg - 1) / kseg != S) continue;                 // S segments must all be non-empty
@@ -1235,35 +1298,34 @@ int launch_gtc_t(const void *wq, int64_t N, int64_t K, const void *x, int M, flo
     // A ring with several column groups streams slower than two launches on halves of the tokens with
     // resident tiles (measured: ffn_down 2560x9728 Q6_K at 7 tokens 25.6 us as a ring); for matrices
     // up to 64 MB the caller halves the tokens instead.
-    if (NT > 1 && best_ns > 0 && N * row_bytes(QT, K) < ((int64_t)64 << 20)) return -3;
+    if (NT > 1 && best_ns > 0 && total_rows * row_bytes(QT, K) < ((int64_t)64 << 20)) return -3;
     if (dry) return 0;                                                // planning only (launch counting)
     const int64_t kseg = ((nmacro + best_s - 1) / best_s) * 256;
-    if constexpr (KWMAX >= 8) if (best_kw == 8) return launch_gtc_kw<QT, NT, XBF16, 8>(wq, N, K, x, M, y, best_s, kseg, best_ns, status, st, stall);
-    if constexpr (KWMAX >= 4) if (best_kw == 4) return launch_gtc_kw<QT, NT, XBF16, 4>(wq, N, K, x, M, y, best_s, kseg, best_ns, status, st, stall);
-    if constexpr (KWMAX >= 2) if (best_kw == 2) return launch_gtc_kw<QT, NT, XBF16, 2>(wq, N, K, x, M, y, best_s, kseg, best_ns, status, st, stall);
-    return launch_gtc_kw<QT, NT, XBF16, 1>(wq, N, K, x, M, y, best_s, kseg, best_ns, status, st, stall);
+    if constexpr (KWMAX >= 8) if (best_kw == 8) return launch_gtc_kw<QT, NT, XBF16, 8>(ms, K, x, M, best_s, kseg, best_ns, status, st, stall, early);
+    if constexpr (KWMAX >= 4) if (best_kw == 4) return launch_gtc_kw<QT, NT, XBF16, 4>(ms, K, x, M, best_s, kseg, best_ns, status, st, stall, early);
+    if constexpr (KWMAX >= 2) if (best_kw == 2) return launch_gtc_kw<QT, NT, XBF16, 2>(ms, K, x, M, best_s, kseg, best_ns, status, st, stall, early);
+    return launch_gtc_kw<QT, NT, XBF16, 1>(ms, K, x, M, best_s, kseg, best_ns, status, st, stall, early);
 }
 
 struct GtcLaunch {
     bool xbf16;
-    const void *wq;
-    int64_t N, K;
+    const MatSet *ms;
+    int64_t K;
     const void *x;
     int M;
-    float *y;
     unsigned int *status;
     cudaStream_t st;
     bool dry;
-    int stall;
+    int stall, early;
     template <int QT> int operator()() {
         if constexpr (QT <= T_BF16) {
             return -1;
         } else {
-            if (xbf16) return M <= 8 ? launch_gtc_t<QT, 1, true>(wq, N, K, x, M, y, status, st, dry, stall)
-                                     : launch_gtc_t<QT, 2, true>(wq, N, K, x, M, y, status, st, dry, stall);
-            if (M <= 4) return launch_gtc_t<QT, 1, false>(wq, N, K, x, M, y, status, st, dry, stall);
-            if (M <= 8) return launch_gtc_t<QT, 2, false>(wq, N, K, x, M, y, status, st, dry, stall);
-            return launch_gtc_t<QT, 4, false>(wq, N, K, x, M, y, status, st, dry, stall);
+            if (xbf16) return M <= 8 ? launch_gtc_t<QT, 1, true>(*ms, K, x, M, status, st, dry, stall, early)
+                                     : launch_gtc_t<QT, 2, true>(*ms, K, x, M, status, st, dry, stall, early);
+            if (M <= 4) return launch_gtc_t<QT, 1, false>(*ms, K, x, M, status, st, dry, stall, early);
+            if (M <= 8) return launch_gtc_t<QT, 2, false>(*ms, K, x, M, status, st, dry, stall, early);
+            return launch_gtc_t<QT, 4, false>(*ms, K, x, M, status, st, dry, stall, early);
         }
     }
 };
@@ -1378,8 +1440,21 @@ struct GtcIdLaunch {
 // cluster allows cannot hold the activations of this many tokens (the caller then halves the group).
 // dry: plan only, launch nothing (0 or -3), for counting launches.
 int launch_gemv_tc(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int M, float *y,
-                   unsigned int *status, cudaStream_t st, bool dry, int stall) {
-    GtcLaunch f{xbf16, wq, N, K, x, M, y, status, st, dry, stall};
+                   unsigned int *status, cudaStream_t st, bool dry, int stall, bool early) {
+    MatSet ms = {};
+    ms.count = 1;
+    ms.wq[0] = wq;
+    ms.N[0] = N;
+    ms.y[0] = y;
+    GtcLaunch f{xbf16, &ms, K, x, M, status, st, dry, stall, early ? 1 : 0};
+    return dispatch_type(qt, f);
+}
+
+// Several matrices of one type and K sharing x in one launch (M <= 16; the matrices' outputs y[i] are
+// M x N[i]). Returns -3 when no work split fits on chip for this many tokens.
+int launch_gemv_tc_multi(int qt, bool xbf16, const MatSet &ms, int64_t K, const void *x, int M,
+                         unsigned int *status, cudaStream_t st, bool dry, bool early) {
+    GtcLaunch f{xbf16, &ms, K, x, M, status, st, dry, 0, early ? 1 : 0};
     return dispatch_type(qt, f);
 }
 

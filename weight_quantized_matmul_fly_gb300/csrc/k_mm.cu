@@ -57,7 +57,7 @@ template <int QT, int T, int J, bool XF32>
 __global__ void __launch_bounds__(THREADS, 1)
     mm_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint8_t *__restrict__ wq, int N, int64_t K,
               int64_t rowbytes, int M, float *__restrict__ y, int ksteps_per_split, float *__restrict__ part,
-              int64_t split_stride, unsigned int *status) {
+              int64_t split_stride, int early, unsigned int *status) {
     constexpr int TN = T * J;
     constexpr int STAGES = stages_of(TN, XF32);
     constexpr int XSLOTS = xslots_of(TN, XF32);
@@ -113,8 +113,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     asm volatile("griddepcontrol.launch_dependents;");
     if (warp == 0) {
         // ---------------- activation producer: the activations may come from the preceding kernel, so
-        // they are loaded only after it has completed (the weights, which no kernel here writes, are
-        // decoded meanwhile)
+        // they are loaded only after it has completed
         asm volatile("griddepcontrol.wait;" ::: "memory");
         if (lane == 0) {
             constexpr int NB = XF32 ? XSLOTS : STAGES;     // ring the loads go to
@@ -183,6 +182,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int nchunks = (int)((K + 31) / 32);
         const uint32_t sA_u32 = ptx::smem_u32(sA), sB_u32 = ptx::smem_u32(sB);
         using SL = Slab<QT>;
+        // Before waiting for the preceding kernel, this row's weights of the split are only prefetched into
+        // L2 (coherent, so never stale even if that kernel wrote them); they are read after the wait. With
+        // `early` (the caller states that the preceding kernel does not write the weights) the decoders
+        // start reading them at once, overlapping the end of that kernel.
+        if (!early && h == 0 && grp == 0 && row_ok && nsteps > 0) {
+            const int64_t cb = (int64_t)kbeg * BK / TypeInfo<QT>::QK, ce = (int64_t)kend * BK / TypeInfo<QT>::QK;
+            const int64_t nb = K / TypeInfo<QT>::QK;
+            const uintptr_t a = reinterpret_cast<uintptr_t>(wrow + cb * TypeInfo<QT>::BYTES);
+            const uintptr_t e = reinterpret_cast<uintptr_t>(wrow + (ce < nb ? ce : nb) * TypeInfo<QT>::BYTES);
+            const uintptr_t wend = reinterpret_cast<uintptr_t>(wq + (int64_t)N * rowbytes);
+            const uintptr_t a0 = a & ~(uintptr_t)15;
+            uintptr_t e1 = (e + 15) & ~(uintptr_t)15;
+            if (e1 > wend) e1 = wend & ~(uintptr_t)15;
+            if (e1 > a0) ptx::prefetch_l2(reinterpret_cast<const void *>(a0), (uint32_t)(e1 - a0));
+        }
+        if (!early) asm volatile("griddepcontrol.wait;" ::: "memory");
         // raw bytes of the group's next PF K steps are in flight while a step is decoded (rw[0] is the
         // step being decoded, rw[PF] the one requested during it)
         typename SL::Raw rw[PF + 1];
@@ -506,7 +521,7 @@ bool mm_attrs() {
 
 template <int QT, int T, int J, bool XF32>
 int launch_mm_t(const void *wq, int64_t N, int64_t K, const void *x, int64_t M, float *y, int S, int kps, float *part,
-                int64_t split_stride, unsigned int *status, cudaStream_t st) {
+                int64_t split_stride, int early, unsigned int *status, cudaStream_t st) {
     constexpr int TN = T * J;
     CUtensorMap map;
     if (!make_x_tmap(&map, x, XF32, M, K, TN > 256 ? 256 : TN)) return -6;
@@ -518,7 +533,7 @@ int launch_mm_t(const void *wq, int64_t N, int64_t K, const void *x, int64_t M, 
     const int Ni = (int)N, Mi = (int)M;
     return launch_pdl(reinterpret_cast<const void *>(kern), grid, dim3(mm::THREADS),
                       (size_t)mm::smem_bytes(TN, XF32), st, part ? 1 : S, map, w8, Ni, K, rb, Mi, y, kps, part,
-                      split_stride, status);
+                      split_stride, early, status);
 }
 
 struct MmLaunch {
@@ -532,6 +547,7 @@ struct MmLaunch {
     int S, kps;
     float *part;
     int64_t split_stride;
+    int early;
     unsigned int *status;
     cudaStream_t st;
     template <int QT, int T, int JJ> int go_j() {
@@ -541,9 +557,10 @@ struct MmLaunch {
         if constexpr (!shape_ok) {
             return -7;
         } else {
-            if (!xf32) return launch_mm_t<QT, T, JJ, false>(wq, N, K, x, M, y, S, kps, part, split_stride, status, st);
+            if (!xf32)
+                return launch_mm_t<QT, T, JJ, false>(wq, N, K, x, M, y, S, kps, part, split_stride, early, status, st);
             if constexpr (TN <= 128)
-                return launch_mm_t<QT, T, JJ, true>(wq, N, K, x, M, y, S, kps, part, split_stride, status, st);
+                return launch_mm_t<QT, T, JJ, true>(wq, N, K, x, M, y, S, kps, part, split_stride, early, status, st);
             return -7;
         }
     }
@@ -662,7 +679,7 @@ size_t mm_partial_bytes(int qt, int64_t N, int64_t K, int64_t M) {
 // scratch of mm_partial_bytes() for the K splits' partial tiles (then the plan is the unclustered one), or
 // nullptr to add them inside a cluster (the clustered plan).
 int launch_mm(int qt, int tile, const void *wq, int64_t N, int64_t K, const void *x, bool x_f32, int64_t M,
-              float *y, float *part, unsigned int *status, cudaStream_t st) {
+              float *y, float *part, bool early, unsigned int *status, cudaStream_t st) {
     const MmPlan plan = mm_plan(qt, N, K, M, part == nullptr);
     const int S = plan.S;
     const int cols = x_f32 && plan.cols > 128 ? 128 : plan.cols;
@@ -670,7 +687,8 @@ int launch_mm(int qt, int tile, const void *wq, int64_t N, int64_t K, const void
     const int kps = (int)((ksteps + S - 1) / S);
     if (S == 1) part = nullptr;
     const int64_t sstride = split_stride_of(M, N);
-    MmLaunch f{tile, tiles_per_cta(tile, M, cols), x_f32, wq, N, K, x, M, y, S, kps, part, sstride, status, st};
+    MmLaunch f{tile, tiles_per_cta(tile, M, cols), x_f32, wq, N, K, x, M, y, S, kps, part, sstride, early ? 1 : 0,
+               status, st};
     int rc = dispatch_type(qt, f);
     if (rc || !part) return rc;
     const int64_t n = M * N, n4 = n / 4;

@@ -86,6 +86,13 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         : "memory");
 }
 
+// Prefetch of `bytes` bytes at `src` (both 16-byte multiples) into L2. L2 is the point of coherence of device
+// memory, so a prefetch issued before the preceding kernel has finished never makes a later read stale.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+                 : "memory");
+}
+
 // ------------------------------------------------------------------------------------------ tcgen05
 // TMEM allocation: a whole warp allocates `ncols` columns (power of two >= 32) and the base address is
 // written to shared memory at `dst`.

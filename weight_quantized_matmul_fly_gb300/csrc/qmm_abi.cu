@@ -15,12 +15,14 @@ __device__ unsigned int g_status = 0;
 int launch_gemv(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int64_t M, float *y,
                 cudaStream_t st);
 int launch_gemv_tc(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int M, float *y,
-                   unsigned int *status, cudaStream_t st, bool dry = false, int stall = 0);
+                   unsigned int *status, cudaStream_t st, bool dry = false, int stall = 0, bool early = false);
+int launch_gemv_tc_multi(int qt, bool xbf16, const MatSet &ms, int64_t K, const void *x, int M,
+                         unsigned int *status, cudaStream_t st, bool dry, bool early);
 int launch_gemv_tc_id(int qt, bool xbf16, const void *const *wq, int64_t E, int64_t N, int64_t K, const void *x,
                       bool x_per_slot, const int32_t *ids, int64_t M, int topk, float *y, unsigned int *status,
                       cudaStream_t st);
 int launch_mm(int qt, int tile, const void *wq, int64_t N, int64_t K, const void *x, bool x_f32, int64_t M,
-              float *y, float *part, unsigned int *status, cudaStream_t st);
+              float *y, float *part, bool early, unsigned int *status, cudaStream_t st);
 size_t mm_partial_bytes(int qt, int64_t N, int64_t K, int64_t M);
 int mm_ksplit(int qt, int64_t N, int64_t K, int64_t M, bool cluster);
 int mm_plan_cols(int qt, int64_t N, int64_t K, int64_t M, bool cluster);
@@ -46,7 +48,7 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 // Common checks of qmm-family arguments. Returns 0 or a QMM_E* code.
 int check_qmm(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, const float *y) {
-    if ((qtype & ~(0xff | QMM_X_BF16)) != 0) return QMM_EQTYPE;
+    if ((qtype & ~(0xff | QMM_X_BF16 | QMM_W_STATIC)) != 0) return QMM_EQTYPE;
     const int qt = qtype & 0xff;
     if (qt < 0 || qt >= T_COUNT) return QMM_EQTYPE;
     if (N <= 0 || K <= 0 || M <= 0 || N >= kMaxDim || K >= kMaxDim || M >= kMaxDim) return QMM_EDIM;
@@ -78,7 +80,7 @@ unsigned int *status_ptr() {
 // halved when the activations of a K segment would not fit on chip); the plain types on the binary32 one.
 // With `launches` non-null nothing is launched: the launches the call would make are counted instead.
 int run_matvec(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const void *x, int64_t M, float *y,
-               cudaStream_t st, int *launches = nullptr, int stall = 0) {
+               cudaStream_t st, int *launches = nullptr, int stall = 0, bool early = false) {
     if (is_plain(qt)) {
         if (launches) { *launches = (int)((M + 15) / 16); return 0; }
         return launch_gemv(qt, xbf16, wq, N, K, x, M, y, st);
@@ -92,7 +94,7 @@ int run_matvec(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const v
         int rc;
         for (;;) {
             rc = launch_gemv_tc(qt, xbf16, wq, N, K, static_cast<const uint8_t *>(x) + m0 * K * esz, mg,
-                                y + m0 * N, status, st, launches != nullptr, m0 == 0 ? stall : 0);
+                                y + m0 * N, status, st, launches != nullptr, m0 == 0 ? stall : 0, early);
             if (rc != -3 || mg <= 4) break;
             mg = (mg + 1) / 2;
         }
@@ -101,6 +103,30 @@ int run_matvec(int qt, bool xbf16, const void *wq, int64_t N, int64_t K, const v
         m0 += mg;
     }
     if (launches) *launches = count;
+    return 0;
+}
+
+// The mat-vec path for several matrices of one type and K that share x: one launch per token group, its
+// CTAs covering the row blocks of every matrix (the groups halved as run_matvec halves them).
+int run_matvec_multi(int qt, bool xbf16, const MatSet &ms, int64_t K, const void *x, int64_t M, cudaStream_t st,
+                     bool early) {
+    const int esz = xbf16 ? 2 : 4;
+    unsigned int *status = status_ptr();
+    if (!status) return QMM_ECUDA;
+    for (int64_t m0 = 0; m0 < M;) {
+        int mg = (int)((M - m0) < 16 ? (M - m0) : 16);
+        MatSet g = ms;
+        for (int i = 0; i < ms.count; ++i) g.y[i] = ms.y[i] + m0 * ms.N[i];
+        int rc;
+        for (;;) {
+            rc = launch_gemv_tc_multi(qt, xbf16, g, K, static_cast<const uint8_t *>(x) + m0 * K * esz, mg, status, st,
+                                      false, early);
+            if (rc != -3 || mg <= 4) break;
+            mg = (mg + 1) / 2;
+        }
+        if (rc) return rc == -3 ? QMM_EDIM : rc;
+        m0 += mg;
+    }
     return 0;
 }
 
@@ -131,21 +157,23 @@ int run_mm(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64
     if (reinterpret_cast<uintptr_t>(ws) & 255u) return QMM_EALIGN;
     unsigned int *status = status_ptr();
     if (!status) return QMM_ECUDA;
-    const bool xf32 = !(qtype & QMM_X_BF16);
+    const bool xf32 = !(qtype & QMM_X_BF16), early = (qtype & QMM_W_STATIC) != 0;
     const size_t need = ws_bytes(qtype, N, K, M, tile);
     if (need && ws && wsb >= need) {
         int rc = launch_x_to_bf16(static_cast<const float *>(x), ws, M * K, st);
         if (rc) return rc;
         float *part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ws_x_bytes(qtype, K, M, tile));
-        return launch_mm(qt, tile, wq, N, K, ws, false, M, y, part, status, st);
+        return launch_mm(qt, tile, wq, N, K, ws, false, M, y, part, early, status, st);
     }
-    return launch_mm(qt, tile, wq, N, K, x, xf32, M, y, nullptr, status, st);
+    return launch_mm(qt, tile, wq, N, K, x, xf32, M, y, nullptr, early, status, st);
 }
 
 // Expert-indexed path for the routing a call carries on average: the tensor-core kernel once an expert
 // gets enough routed pairs that decoding its weights once per pass of up to 32-128 pairs beats the mat-vec
-// machinery's passes of 4 (8 with bf16 activations) pairs.
-constexpr int64_t kIdTensorMinPairs = 16;
+// machinery's passes of 4 (8 with bf16 activations) pairs. Measured on GB300 (128 experts of 4096 x K Q4_0,
+// K = 512-1024, top-8): the mat-vec kernel is faster up to at least 16 pairs per expert (256 tokens); the
+// threshold sits above that.
+constexpr int64_t kIdTensorMinPairs = 48;
 int pick_id_path(int qt, int64_t E, int64_t K, int64_t M, int topk) {
     const int64_t nslot = M * topk, used = nslot < E ? nslot : E;
     return (mm_eligible(qt, K) && nslot >= kIdTensorMinPairs * used) ? 2 : 1;
@@ -153,7 +181,7 @@ int pick_id_path(int qt, int64_t E, int64_t K, int64_t M, int topk) {
 
 int run_qmm_id(const void *const *wq, int64_t E, int qtype, int64_t N, int64_t K, const void *x, const int32_t *ids,
                int64_t M, int topk, float *y, void *stream, int path) {
-    if ((qtype & ~(0xff | QMM_X_BF16 | QMM_X_PER_SLOT)) != 0) return QMM_EQTYPE;
+    if ((qtype & ~(0xff | QMM_X_BF16 | QMM_X_PER_SLOT | QMM_W_STATIC)) != 0) return QMM_EQTYPE;
     const int qt = qtype & 0xff;
     if (qt < 0 || qt >= T_COUNT) return QMM_EQTYPE;
     if (N <= 0 || K <= 0 || M <= 0 || N >= kMaxDim || K >= kMaxDim) return QMM_EDIM;
@@ -220,7 +248,9 @@ int qmm_ws(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64
     if (rc) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int path = qmm_pick_path(qtype, N, K, M);
-    if (path == 0) return run_matvec(qtype & 0xff, (qtype & QMM_X_BF16) != 0, wq, N, K, x, M, y, st);
+    if (path == 0)
+        return run_matvec(qtype & 0xff, (qtype & QMM_X_BF16) != 0, wq, N, K, x, M, y, st, nullptr, 0,
+                          (qtype & QMM_W_STATIC) != 0);
     const size_t need = ws_bytes(qtype, N, K, M, path);
     if (need && (!workspace || workspace_bytes < need)) return QMM_EWORKSPACE;
     return run_mm(wq, qtype, N, K, x, M, y, path, workspace, workspace_bytes, st);
@@ -231,8 +261,37 @@ int qmm(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t 
     if (rc) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int path = qmm_pick_path(qtype, N, K, M);
-    if (path == 0) return run_matvec(qtype & 0xff, (qtype & QMM_X_BF16) != 0, wq, N, K, x, M, y, st);
+    if (path == 0)
+        return run_matvec(qtype & 0xff, (qtype & QMM_X_BF16) != 0, wq, N, K, x, M, y, st, nullptr, 0,
+                          (qtype & QMM_W_STATIC) != 0);
     return run_mm(wq, qtype, N, K, x, M, y, path, nullptr, 0, st);
+}
+
+int qmm_batch(int count, const void *const *wq, const int64_t *N, float *const *y, int qtype, int64_t K,
+              const void *x, int64_t M, void *stream) {
+    if (count < 1 || count > kMaxBatch) return QMM_ERANGE;
+    if (!wq || !N || !y) return QMM_ENULL;
+    for (int i = 0; i < count; ++i) {
+        const int rc = check_qmm(wq[i], qtype, N[i], K, x, M, y[i]);
+        if (rc) return rc;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int qt = qtype & 0xff;
+    if (M <= kGemvMaxM && !is_plain(qt) && count > 1) {
+        MatSet ms = {};
+        ms.count = count;
+        for (int i = 0; i < count; ++i) {
+            ms.wq[i] = wq[i];
+            ms.N[i] = N[i];
+            ms.y[i] = y[i];
+        }
+        return run_matvec_multi(qt, (qtype & QMM_X_BF16) != 0, ms, K, x, M, st, (qtype & QMM_W_STATIC) != 0);
+    }
+    for (int i = 0; i < count; ++i) {
+        const int rc = qmm(wq[i], qtype, N[i], K, x, M, y[i], stream);
+        if (rc) return rc;
+    }
+    return 0;
 }
 
 int qmm_with_tile(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, float *y, int tile,
@@ -240,7 +299,9 @@ int qmm_with_tile(const void *wq, int qtype, int64_t N, int64_t K, const void *x
     int rc = check_qmm(wq, qtype, N, K, x, M, y);
     if (rc) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (tile == 0) return run_matvec(qtype & 0xff, (qtype & QMM_X_BF16) != 0, wq, N, K, x, M, y, st);
+    if (tile == 0)
+        return run_matvec(qtype & 0xff, (qtype & QMM_X_BF16) != 0, wq, N, K, x, M, y, st, nullptr, 0,
+                          (qtype & QMM_W_STATIC) != 0);
     if (tile != 32 && tile != 64 && tile != 128) return QMM_ERANGE;
     if (!mm_eligible(qtype & 0xff, K)) return QMM_EBLOCK;
     return run_mm(wq, qtype, N, K, x, M, y, tile, nullptr, 0, st);

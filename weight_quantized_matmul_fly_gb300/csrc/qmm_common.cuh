@@ -394,6 +394,16 @@ __host__ __device__ __forceinline__ int64_t row_bytes(int qt, int64_t K) {
     return (K / qk[qt]) * nb[qt];
 }
 
+// Host-side list of weight matrices of one type and K that share their activations (one mat-vec launch
+// serves them all); count = 1 for a single matrix.
+constexpr int kMaxBatch = 8;
+struct MatSet {
+    int count;
+    const void *wq[kMaxBatch];
+    int64_t N[kMaxBatch];
+    float *y[kMaxBatch];
+};
+
 // Dispatch a functor templated on the weight type.
 template <typename F>
 inline int dispatch_type(int qt, F &&f) {

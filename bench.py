@@ -261,11 +261,13 @@ def run_ours(args):
     P = ctypes.c_void_p
 
     ncalls = len(calls)
+    names = {c[0] for c in calls}
     per_step_launches = sum(qmm.qmm_launch_count(c[3], c[1], c[2], c[4]) for c in calls
-                            if not (c[4] <= 16 and c[0] in SHARED_PARTNERS))
+                            if not (c[4] <= 16 and c[0] in SHARED_PARTNERS and
+                                    any(SHARED_INPUT.get(n) == c[0] for n in names)))
 
-    # One CUDA graph per (weight copy, token-count group): the group's calls are captured back to back, so
-    # consecutive kernels overlap through programmatic dependent launch; events sit only between groups.
+    # The calls grouped by token count (the 65-token batch of two is one group); inside a captured graph
+    # consecutive kernels overlap through programmatic dependent launch.
     groups = []                                   # list of (label, [call indices])
     for i, c in enumerate(calls):
         label = "%dx%d" % (2, c[4]) if c[4] == BATCH2 else str(c[4])
@@ -280,9 +282,9 @@ def run_ours(args):
                 continue
             name, N, K, qt, M, b = calls[i]
             partner = SHARED_INPUT.get(name)
-            if M <= 16 and partner is not None:
+            j = next((j for j in idxs if partner and calls[j][0] == partner and calls[j][5] == b), None)
+            if M <= 16 and j is not None:
                 # the projections that share this input and type: one mat-vec launch (qmm_batch)
-                j = next(j for j in idxs if calls[j][0] == partner and calls[j][5] == b)
                 done.add(j)
                 N2 = calls[j][1]
                 qmm.qmm_batch([wq[(copy, name)], wq[(copy, partner)]], qmm.TYPE_ID[qt] | qmm.W_STATIC, [N, N2], K,
@@ -298,24 +300,36 @@ def run_ours(args):
         for _, idxs in groups:
             run_group(s % COPIES, idxs)
     torch.cuda.synchronize()
-    graphs = {}
+    # The timed steps: one CUDA graph per weight copy holding the whole step (all groups back to back), the
+    # copies replayed in turn. Per-group times: one graph per group holding that group for every weight copy
+    # (the layer at that token count seven times over, as a model runs its layers), replayed in steady state;
+    # they give the per-token-count figures and the roofline classes.
+    graphs, ggraphs = {}, {}
     with torch.cuda.stream(stream):
         for copy in range(COPIES):
-            for gi, (_, idxs) in enumerate(groups):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _, idxs in groups:
                     run_group(copy, idxs)
-                graphs[(copy, gi)] = g
+            graphs[copy] = g
+        for gi, (_, idxs) in enumerate(groups):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for copy in range(COPIES):
+                    run_group(copy, idxs)
+            ggraphs[gi] = g
     torch.cuda.synchronize()
     for s in range(args.warmup):                  # warm-up replays
+        graphs[s % COPIES].replay()
         for gi in range(len(groups)):
-            graphs[(s % COPIES, gi)].replay()
+            ggraphs[gi].replay()
     torch.cuda.synchronize()
 
     ng = len(groups)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(ng + 1)] for _ in range(args.steps)]
     t0e = torch.cuda.Event(enable_timing=True)
     t1e = torch.cuda.Event(enable_timing=True)
+    gev = [torch.cuda.Event(enable_timing=True) for _ in range(ng + 1)]
+    greps = max(2, args.steps // COPIES)
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
@@ -323,21 +337,18 @@ def run_ours(args):
         with Clocks(local) as clk:
             t0e.record(stream)
             for s in range(args.steps):
-                copy = (args.warmup + s) % COPIES
-                for gi in range(ng):
-                    evs[s][gi].record(stream)
-                    graphs[(copy, gi)].replay()
-                evs[s][ng].record(stream)
+                graphs[(args.warmup + s) % COPIES].replay()
             t1e.record(stream)
+            for gi in range(ng):
+                gev[gi].record(stream)
+                for _ in range(greps):
+                    ggraphs[gi].replay()
+            gev[ng].record(stream)
             torch.cuda.synchronize()
     if pg:
         pg.barrier()
     total_ms = max_over_ranks(pg, t0e.elapsed_time(t1e), dev)
-    group_ms = np.zeros(ng)
-    for s in range(args.steps):
-        for gi in range(ng):
-            group_ms[gi] += evs[s][gi].elapsed_time(evs[s][gi + 1])
-    group_ms /= args.steps
+    group_ms = np.array([gev[gi].elapsed_time(gev[gi + 1]) / (greps * COPIES) for gi in range(ng)])
     # per-call times are not measured inside a group; spread each group's time over its calls by weight
     # bytes for the per-call table only (the aggregates below use group times)
     call_ms = np.zeros(ncalls)
@@ -397,6 +408,8 @@ def run_ours(args):
         del d["wbytes"], d["flops"], d["roof"]
 
     if args.detail:
+        print("step %.2f us (whole-step graphs), sum of steady-state groups %.2f us" % (
+            total_ms / args.steps * 1e3, group_ms.sum() * 1e3), file=sys.stderr)
         for gi, (label, idxs) in enumerate(groups):
             wb = sum(weight_bytes(calls[i][1], calls[i][2], calls[i][3]) for i in idxs)
             fl = sum(2.0 * calls[i][4] * calls[i][1] * calls[i][2] for i in idxs)
@@ -405,7 +418,7 @@ def run_ours(args):
                 fl / (group_ms[gi] * 1e-3) / 1e12), file=sys.stderr)
     unbatched = run_unbatched(args, qmm, torch, dev, wq, peaks) if not args.case else None
     e2e = run_e2e(args, qmm, torch, dev, calls, wq, ws) if not args.case else None
-    del wq, xs, ys, graphs
+    del wq, xs, ys, graphs, ggraphs
     torch.cuda.empty_cache()
     extra = not args.case and not args.no_extra
     moe = run_moe(args, qmm, torch, dev, peaks) if (not args.case and not args.no_moe) else None

@@ -182,7 +182,7 @@ int qmm_id(const void *const *wq, int64_t E, int qtype, int64_t N, int64_t K, co
 
 /* Which kernel qmm_id runs (qmm_id_pick_path): 1 = the expert-indexed mat-vec (binary32 products of the
  * exactly rounded weights, tolerance class 1e-5), used while an expert gets few routed pairs on average
- * (M*topk < 48 * min(E, M*topk)); 2 = the tensor-core expert kernel (x and weights rounded to bfloat16,
+ * (M*topk < 128 * min(E, M*topk)); 2 = the tensor-core expert kernel (x and weights rounded to bfloat16,
  * tolerance class 4e-3, like qmm's tensor-core path): each CTA takes one row block of one distinct expert
  * and runs tcgen05 MMAs over passes of up to 32/64/128 of its routed pairs, the activation rows gathered
  * by bulk copies, so each pass decodes the expert's weights once for all of them. Path 2 needs K a

@@ -145,7 +145,7 @@ def test_qmm_id_path_choice(L):
     assert qmm.qmm_id_pick_path("Q4_0", 128, 512, 24, 8) == 1
     assert qmm.qmm_id_pick_path("Q4_0", 128, 512, 256, 8) == 1
     assert qmm.qmm_id_pick_path("Q4_0", 16, 512, 256, 8) == 2
-    assert qmm.qmm_id_pick_path("F32", 2, 256, 64, 2) == 2
+    assert qmm.qmm_id_pick_path("F32", 1, 256, 128, 1) == 2
     ptrs = (ctypes.c_void_p * 2)(A, A)
     arr = ctypes.cast(ptrs, P)
     assert L.qmm_id_with_path(arr, 2, 3, 64, 64, P(A), P(A), 1, 8, P(A), 3, None) == -7   # no such path

@@ -78,18 +78,16 @@ def test_qmm_id_long_k_cluster_split():
 
 @pytest.mark.parametrize("bf16", [False, True])
 def test_qmm_id_many_slots_per_expert(bf16):
-    """64 tokens over 4 experts (about 64 slots each). qmm_id picks the tensor-core expert kernel there
-    (bf16 class); forced onto the mat-vec expert kernel the call runs many passes of 4 (8 for bf16
-    activations) tokens (binary32 class)."""
+    """64 tokens over 4 experts (about 64 slots each): on the tensor-core expert kernel (bf16 class), and on
+    the mat-vec expert kernel, many passes of 4 (8 for bf16 activations) tokens (binary32 class)."""
     from gpu_util import TOL_BF16
     E, N, K, M, topk = 4, 96, 512, 64, 4
     wqs = _experts("Q4_K", E, N, K, seed=5)
     x = synthetic.activations(M, K, seed=5, bf16=bf16)
     ids = synthetic.expert_ids(M, E=E, topk=topk, seed=5)
     ref, bnd = oracle.qmm_id("Q4_K", wqs, N, K, x, ids)
-    assert qmm.qmm_id_pick_path("Q4_K", E, K, M, topk) == 2
-    y = _run(wqs, "Q4_K", N, K, x, ids)
-    check_tol(y, ref, bnd, TOL_BF16, "many slots, auto, bf16=%s" % bf16)
+    y = _run_path(wqs, "Q4_K", N, K, x, ids, 2)
+    check_tol(y, ref, bnd, TOL_BF16, "many slots, tensor-core, bf16=%s" % bf16)
     y1 = _run_path(wqs, "Q4_K", N, K, x, ids, 1)
     check_tol(y1, ref, bnd, TOL_FP32, "many slots, mat-vec, bf16=%s" % bf16)
 
@@ -142,7 +140,7 @@ def test_qmm_id_tensor_core_128_experts(n):
     check_tol(y2, ref, bnd, TOL_BF16, "tensor-core n=%d" % n)
     y1 = _run_path(wqs, "Q4_0", N, K, x, ids, 1)
     check_tol(y1, ref, bnd, TOL_FP32, "mat-vec n=%d" % n)
-    assert qmm.qmm_id_pick_path("Q4_0", E, K, n, topk) == (2 if n * topk >= 48 * min(E, n * topk) else 1)
+    assert qmm.qmm_id_pick_path("Q4_0", E, K, n, topk) == (2 if n * topk >= 128 * min(E, n * topk) else 1)
 
 
 @pytest.mark.parametrize("qtype", ["Q4_K", "Q6_K", "Q8_0", "A4G64", "Q5_1", "F16", "F32"])
@@ -159,7 +157,6 @@ def test_qmm_id_tensor_core_types_and_passes(qtype):
     ref, bnd = oracle.qmm_id(qtype, wqs, N, K, x, ids)
     y = _run_path(wqs, qtype, N, K, x, ids, 2)
     check_tol(y, ref, bnd, TOL_BF16, qtype)
-    assert qmm.qmm_id_pick_path(qtype, E, K, M, topk) == 2
 
 
 @pytest.mark.parametrize("bf16", [False, True])

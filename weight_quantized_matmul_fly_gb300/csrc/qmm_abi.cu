@@ -170,10 +170,10 @@ int run_mm(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64
 
 // Expert-indexed path for the routing a call carries on average: the tensor-core kernel once an expert
 // gets enough routed pairs that decoding its weights once per pass of up to 32-128 pairs beats the mat-vec
-// machinery's passes of 4 (8 with bf16 activations) pairs. Measured on GB300 (128 experts of 4096 x K Q4_0,
-// K = 512-1024, top-8): the mat-vec kernel is faster up to at least 16 pairs per expert (256 tokens); the
-// threshold sits above that.
-constexpr int64_t kIdTensorMinPairs = 48;
+// machinery's passes of 4 (8 with bf16 activations) pairs. Measured on GB300 (experts of 4096 x K Q4_0,
+// K = 512-1024, top-8): the mat-vec kernel is faster up to 16 pairs per expert (128 experts, 256 tokens) and
+// at 32; the two break even at 128 pairs per expert, and the tensor-core kernel is ahead (5 %) at 256.
+constexpr int64_t kIdTensorMinPairs = 128;
 int pick_id_path(int qt, int64_t E, int64_t K, int64_t M, int topk) {
     const int64_t nslot = M * topk, used = nslot < E ? nslot : E;
     return (mm_eligible(qt, K) && nslot >= kIdTensorMinPairs * used) ? 2 : 1;

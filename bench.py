@@ -23,7 +23,7 @@ weights (qwen3_06b), the expert-indexed product (moe) and the all-type sweep (sw
 The e2e figure times the M <= 16 calls through the C-ABI with activations copied from pinned host memory and
 results copied back inside the timed region.
 
-    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference] [--case NAME:M]
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference] [--case NAME:M | moe:N]
                     [--no-cpu] [--no-moe] [--no-extra] [--detail]
 """
 from __future__ import annotations
@@ -228,6 +228,12 @@ def run_ours(args):
     qmm.build()
     peaks = load_peaks()
 
+    if args.case and args.case.startswith("moe:"):
+        if rank == 0:
+            run_moe_case(args, qmm, torch, dev, peaks, int(args.case.split(":")[1]))
+        if pg:
+            pg.destroy_process_group()
+        return
     calls = calls_of_step()
     if args.case:
         name, m = args.case.split(":")
@@ -446,6 +452,38 @@ def run_ours(args):
         print(json.dumps(line))
     if pg:
         pg.destroy_process_group()
+
+
+def run_moe_case(args, qmm, torch, dev, peaks, n):
+    """One expert-indexed workload alone (--case moe:N): N tokens routed top-8 over 128 experts of
+    4096 x 1024 Q4_0 (one bank), each expert path called once eagerly in the order 2, 1, 2 (a profiler takes
+    the first launch of a kernel), then both paths timed over 16 replayed calls on 8 rotating id tables."""
+    E, Nr, TOPK, K = synthetic.MOE_EXPERTS, synthetic.MOE_ROWS, synthetic.MOE_TOPK, 1024
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    rb = qmm.row_bytes("Q4_0", K)
+    bank = []
+    for _ in range(E):
+        w = torch.randn(Nr, K, device=dev, generator=gen) * 0.02
+        b = torch.empty(rb * Nr, dtype=torch.uint8, device=dev)
+        qmm.qmm_quantize(w, "Q4_0", Nr, K, b)
+        bank.append(b)
+    idss = [torch.from_numpy(synthetic.expert_ids(n, batch=b)).to(dev) for b in range(8)]
+    x = torch.randn(n, K, device=dev, generator=gen)
+    y = torch.empty(n, TOPK, Nr, device=dev)
+    for path in (2, 1, 2):
+        qmm.qmm_id(bank, "Q4_0", Nr, K, x, idss[0], y, path=path)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    row = {"workload": "moe %d tokens, top-8 of 128 experts 4096x1024 Q4_0" % n,
+           "auto_path": qmm.qmm_id_pick_path("Q4_0", E, K, n, TOPK)}
+    for path in (1, 2):
+        fns = [(lambda i=i, path=path: qmm.qmm_id(bank, "Q4_0", Nr, K, x, idss[i % 8], y, path=path))
+               for i in range(16)]
+        us = time_graph(torch, stream, fns)
+        row["us_path%d" % path] = round(us, 2)
+        row["tflops_path%d" % path] = round(2.0 * n * TOPK * Nr * K / us / 1e6, 2)
+    print(json.dumps(row))
 
 
 def time_graph(torch, stream, calls, replays=4):
@@ -857,7 +895,7 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--case", default=None, help="time one call only, e.g. ffn_gate:2048")
+    ap.add_argument("--case", default=None, help="time one call only, e.g. ffn_gate:2048, or one expert-indexed workload, e.g. moe:256")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--detail", action="store_true", help="per-call device times on stderr")
     ap.add_argument("--no-moe", action="store_true", help="skip the expert-indexed (MoE) leg")

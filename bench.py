@@ -55,23 +55,38 @@ WORKLOAD = ("Qwen3-Embedding-4B layer: attn_q 4096x2560 Q4_K, attn_k 1024x2560 Q
             "weights N(0,0.02) quantized")
 
 
-# DRAM traffic per launch of the dominant kernel, from one ncu capture of the bench's own step
-# (dram__bytes_read.sum + dram__bytes_write.sum averaged over the kernel's launches in the class the
-# roofline object reports). Valid only for the kernel source it was taken on: None once that changed.
-TRAFFIC = {"class": None, "bytes_per_launch": None, "launches": 0,
-           "source": "weight_quantized_matmul_fly_gb300/csrc/k_mm.cu", "sha256": None}
+# DRAM traffic of the dominant call class, from one ncu capture of the bench's own step
+# (dram__bytes_read.sum + dram__bytes_write.sum of every launch, attributed to the calls in launch order;
+# one pass): bytes per call over all the class's launches (the tensor-core kernel and its helper kernels),
+# with the algorithmic bytes per call (weights + binary32 activations) and launches per call beside it.
+# Valid only for the kernel and planner sources it was taken on: None once one of them has changed.
+TRAFFIC = {"class": "m_17_136", "bytes_per_call": 16.16e6, "algorithmic_bytes_per_call": 10.415e6,
+           "launches_per_call": 2.8, "mm_kernel_bytes_per_call": 9.841e6,
+           "sources": ["weight_quantized_matmul_fly_gb300/csrc/k_mm.cu", "weight_quantized_matmul_fly_gb300/csrc/mm_slab.cuh",
+                       "weight_quantized_matmul_fly_gb300/csrc/ptx.cuh", "weight_quantized_matmul_fly_gb300/csrc/qmm_abi.cu"],
+           "sha256": "cd1158b712873aa05d5692182aba89639a4002bf1f2976748eab83dd120c6e5b"}
+
+
+def sources_digest(paths):
+    import hashlib
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
 
 
 def recorded_traffic(cls):
-    """The recorded DRAM bytes per launch for this call class, or None (not measured on this source)."""
-    import hashlib
+    """The recorded DRAM traffic of this call class, or None (not measured on these sources)."""
     if TRAFFIC["class"] != cls or not TRAFFIC["sha256"]:
         return None
     try:
-        h = hashlib.sha256(open(os.path.join(ROOT, TRAFFIC["source"]), "rb").read()).hexdigest()
+        if sources_digest(TRAFFIC["sources"]) != TRAFFIC["sha256"]:
+            return None
     except OSError:
         return None
-    return TRAFFIC["bytes_per_launch"] if h == TRAFFIC["sha256"] else None
+    return {k: TRAFFIC[k] for k in ("bytes_per_call", "algorithmic_bytes_per_call", "launches_per_call",
+                                    "mm_kernel_bytes_per_call")}
 
 
 def load_peaks():
@@ -389,14 +404,16 @@ def run_ours(args):
     bound = d["bound"]
     peak = peaks["hbm_gbs"] if bound == "hbm" else peaks["bf16_tflops"]
     roof = {"bound": bound, "achieved": round(d["frac"] * peak, 2), "peak": peak,
-            "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "frac": d["frac"], "traffic": recorded_traffic(dom),
+            "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "frac": d["frac"],
+            "traffic": (recorded_traffic(dom) or {}).get("bytes_per_call"), "traffic_detail": recorded_traffic(dom),
             "class": dom, "kernel": ("gtc::gemv_tc_kernel (mma.sync mat-vec)" if dom == "m_le_16"
                                      else "mm::mm_kernel (tcgen05) with its helper kernels"),
             "peak_kind": ("HBM copy" if bound == "hbm" else "bf16 dense, burst") + ", " + peaks["source"],
             "achieved_kind": "sum of per-call roofline times / measured time, times the peak of the bound "
                              "that holds for most of the class's roofline time",
             "algorithmic_per_call": "max((N*K*bpw/8 + M*K*4) / HBM, 2*M*N*K / bf16 peak)",
-            "traffic_unit": "DRAM bytes per launch of the kernel (ncu), null unless measured on this source"}
+            "traffic_unit": "DRAM bytes per call of the class over all its launches (ncu over the bench's step), "
+                            "null unless measured on the current kernel and planner sources"}
 
     per_m = {}
     for i, c in enumerate(calls):

@@ -49,7 +49,7 @@ inline int device_sm_count() {
     const int d = current_device_index();
     if (!nsm[d]) {
         int v = 0;
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || v <= 0) return 148;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || v <= 0) return 152;   // no device: plan for a GB300
         nsm[d] = v;
     }
     return nsm[d];

@@ -33,6 +33,8 @@ def test_noalloc_matches_qmm_twice(qtype, N, K, M):
     assert need <= qmm.NOALLOC_SCRATCH_BYTES
     if M > 32:
         assert need >= M * K * 2          # these cases use the array
+    if qtype == "Q6_K":
+        assert qmm.qmm_plan_info(qtype, N, K, M)[1] > 1      # the plan splits K
     wq_h = oracle.quantize(qtype, synthetic.weights(N, K, seed=N + M))
     wq = dev(wq_h)
     tol = TOL_FP32 if M <= 16 else TOL_BF16
@@ -51,6 +53,33 @@ def test_noalloc_matches_qmm_twice(qtype, N, K, M):
         _, bnd = oracle.qmm_sampled(qtype, wq_h, N, K, x_h, ms, ns)
         check_tol(a[ms, ns], b[ms, ns].astype(np.float64), bnd, tol, "noalloc vs qmm, call %d" % call)
         assert np.all(np.isfinite(a))
+
+
+def test_noalloc_allocates_nothing_in_a_graph():
+    """Two qmm_noalloc calls (one using the static array) captured in a CUDA graph after a warm-up call:
+    replaying the graph leaves the device's free memory unchanged."""
+    torch = torch_cuda()
+    qmm.build()
+    qtype, N, K = "Q4_K", 1024, 2560
+    wq = dev(oracle.quantize(qtype, synthetic.weights(N, K, seed=3)))
+    xs = [dev(synthetic.activations(M, K, seed=M)) for M in (7, 100)]
+    ys = [torch.empty((x.shape[0], N), dtype=torch.float32, device="cuda") for x in xs]
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        for x, y in zip(xs, ys):
+            qmm.qmm_noalloc(wq, qtype, N, K, x, y, stream=st)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        for x, y in zip(xs, ys):
+            qmm.qmm_noalloc(wq, qtype, N, K, x, y, stream=st)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert all(bool(torch.isfinite(y).all()) for y in ys)
 
 
 def test_noalloc_refuses_oversized_scratch():

@@ -67,12 +67,12 @@ def test_noalloc_allocates_nothing_in_a_graph():
     st = torch.cuda.Stream()
     with torch.cuda.stream(st):
         for x, y in zip(xs, ys):
-            qmm.qmm_noalloc(wq, qtype, N, K, x, y, stream=st)
+            qmm.qmm_noalloc(wq, qtype, N, K, x, y)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=st):
         for x, y in zip(xs, ys):
-            qmm.qmm_noalloc(wq, qtype, N, K, x, y, stream=st)
+            qmm.qmm_noalloc(wq, qtype, N, K, x, y)
     torch.cuda.synchronize()
     free0 = torch.cuda.mem_get_info()[0]
     for _ in range(3):

@@ -92,7 +92,8 @@ def _qt(qtype) -> int:
 
 def _stream(stream):
     if stream is not None:
-        return ctypes.c_void_p(int(stream))
+        # a torch.cuda.Stream, or a raw cudaStream_t as an integer
+        return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
     import torch
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 

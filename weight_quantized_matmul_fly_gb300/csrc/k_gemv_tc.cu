@@ -899,8 +899,8 @@ __global__ void __launch_bounds__(256, 2)
     const int rg = warp / KW, ks = warp % KW;
     const int nrow0 = blockIdx.x * (16 * RG) + 16 * rg;
 
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (S > 1) cluster_arrive_relaxed();              // matched by the wait before the partials move
 
     // ---- routing: distinct experts in ascending id order, and the slots routed to this CTA's expert.

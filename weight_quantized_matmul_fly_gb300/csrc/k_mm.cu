@@ -385,10 +385,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // y[i] = sum over s of part[s][i], s ascending (the K splits' partial tiles added in split order).
+// This kernel and the conversion below let the next kernel in the stream launch at once (it waits for them
+// before it touches what they write), so the next tensor-core kernel's prologue and first weight loads
+// overlap them; they read their inputs only after the kernel before them has completed.
 __global__ void splitk_reduce_kernel(const float4 *__restrict__ part, int64_t stride4, int S, float4 *__restrict__ y,
                                      int64_t n4) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
         float4 a = part[i];
         for (int s = 1; s < S; ++s) {
@@ -400,8 +403,8 @@ __global__ void splitk_reduce_kernel(const float4 *__restrict__ part, int64_t st
 }
 __global__ void splitk_reduce_tail_kernel(const float *__restrict__ part, int64_t stride, int S, float *__restrict__ y,
                                           int64_t beg, int64_t n) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int64_t i = beg + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         float a = part[i];
         for (int s = 1; s < S; ++s) a += part[i + s * stride];
@@ -411,8 +414,8 @@ __global__ void splitk_reduce_tail_kernel(const float *__restrict__ part, int64_
 
 // binary32 -> bfloat16 (round to nearest even), 8 elements per thread; n is a multiple of 8.
 __global__ void x_to_bf16_kernel(const float4 *__restrict__ x, uint4 *__restrict__ out, int64_t n8) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
         const float4 a = x[2 * i], b = x[2 * i + 1];
         out[i] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),

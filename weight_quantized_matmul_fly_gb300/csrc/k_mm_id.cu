@@ -73,8 +73,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     // The routing table usually comes from the preceding kernel (the router), and y may be read by it:
     // wait for it before anything else.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // ---- routing: distinct experts in ascending id order; this CTA's expert and its slots
     for (int i = tid; i < QMM_MAX_EXPERTS; i += THREADS) s_used[i] = 0;

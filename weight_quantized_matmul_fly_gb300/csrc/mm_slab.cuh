@@ -188,5 +188,149 @@ template <> struct Slab<T_Q4_0> {
     }
 };
 
+// ---- legacy 32-weight blocks and the 16-bit plain types: chunk c is block c (resp. weights 32c .. 32c+31).
+// Codes 0..15 of a 4-bit block are the low nibbles of its 16 code bytes, 16..31 the high nibbles; the fifth
+// bit of weight j (Q5_0, Q5_1) is bit j of the 32-bit field qh.
+
+// The four bits (f >> 4i) & 15 moved to bit 4 of bytes 0..3.
+__device__ __forceinline__ uint32_t fifth_bits(uint32_t f, int i) {
+    return ((((f >> (4 * i)) & 15u) * 0x00204081u) & 0x01010101u) << 4;
+}
+// the four codes of v4 (bytes < 128) -> bf16x2 of d * q + m, each the binary32 fma rounded once (exact
+// weights: q is recovered exactly as (128 + q) - 128)
+__device__ __forceinline__ void fma4_pack_m(uint32_t v4, float d, float m, uint32_t &lo, uint32_t &hi) {
+    lo = pack_bf16x2(__fmaf_rn(d, code128(v4, 0) - 128.0f, m), __fmaf_rn(d, code128(v4, 1) - 128.0f, m));
+    hi = pack_bf16x2(__fmaf_rn(d, code128(v4, 2) - 128.0f, m), __fmaf_rn(d, code128(v4, 3) - 128.0f, m));
+}
+
+// Q4_1: 20-byte blocks (4-byte aligned): d, m (binary16), 16 code bytes.
+template <> struct Slab<T_Q4_1> {
+    static constexpr bool FAST = true;
+    struct Raw { uint32_t dm; uint32_t q[4]; };
+    __device__ static void load(Raw &r, const uint8_t *row, int c) {
+        const uint8_t *b = row + 20 * c;
+        r.dm = ld_u32(b);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) r.q[i] = ld_u32(b + 4 + 4 * i);
+    }
+    __device__ static void decode(const Raw &r, int c, uint32_t (&o)[16]) {
+        (void)c;
+        const float d = h2f(r.dm & 0xffffu), m = h2f(r.dm >> 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            fma4_pack_m(r.q[i] & 0x0F0F0F0Fu, d, m, o[2 * i], o[2 * i + 1]);
+            fma4_pack_m((r.q[i] >> 4) & 0x0F0F0F0Fu, d, m, o[8 + 2 * i], o[8 + 2 * i + 1]);
+        }
+    }
+};
+
+// Q5_0: 22-byte blocks (2-byte aligned): d, qh (32 bits), 16 code bytes; w = d * (q - 16), exact as
+// d * (128 + q) - 144 * d (both terms exact).
+template <> struct Slab<T_Q5_0> {
+    static constexpr bool FAST = true;
+    struct Raw { uint32_t d, qh; uint32_t q[4]; };
+    __device__ static void load(Raw &r, const uint8_t *row, int c) {
+        const uint8_t *b = row + 22 * c;
+        r.d = ld_u16(b);
+        r.qh = ld_u16(b + 2) | (ld_u16(b + 4) << 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) r.q[i] = ld_u16(b + 6 + 4 * i) | (ld_u16(b + 8 + 4 * i) << 16);
+    }
+    __device__ static void decode(const Raw &r, int c, uint32_t (&o)[16]) {
+        (void)c;
+        const float d = h2f(r.d), cb = -144.0f * d;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            fma4_pack((r.q[i] & 0x0F0F0F0Fu) | fifth_bits(r.qh, i), d, cb, o[2 * i], o[2 * i + 1]);
+            fma4_pack(((r.q[i] >> 4) & 0x0F0F0F0Fu) | fifth_bits(r.qh >> 16, i), d, cb, o[8 + 2 * i], o[8 + 2 * i + 1]);
+        }
+    }
+};
+
+// Q5_1: 24-byte blocks (8-byte aligned): d, m, qh, 16 code bytes; w = d * q + m.
+template <> struct Slab<T_Q5_1> {
+    static constexpr bool FAST = true;
+    struct Raw { uint32_t dm, qh; uint32_t q[4]; };
+    __device__ static void load(Raw &r, const uint8_t *row, int c) {
+        const uint8_t *b = row + 24 * c;
+        r.dm = ld_u32(b);
+        r.qh = ld_u32(b + 4);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) r.q[i] = ld_u32(b + 8 + 4 * i);
+    }
+    __device__ static void decode(const Raw &r, int c, uint32_t (&o)[16]) {
+        (void)c;
+        const float d = h2f(r.dm & 0xffffu), m = h2f(r.dm >> 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            fma4_pack_m((r.q[i] & 0x0F0F0F0Fu) | fifth_bits(r.qh, i), d, m, o[2 * i], o[2 * i + 1]);
+            fma4_pack_m(((r.q[i] >> 4) & 0x0F0F0F0Fu) | fifth_bits(r.qh >> 16, i), d, m, o[8 + 2 * i], o[8 + 2 * i + 1]);
+        }
+    }
+};
+
+// Q8_0: 34-byte blocks (2-byte aligned): d, 32 signed code bytes; w = d * q, exact as d * u - 128 * d with
+// u = q + 128 (the byte with its top bit flipped) read as 2^23 + u and the bias subtracted exactly.
+template <> struct Slab<T_Q8_0> {
+    static constexpr bool FAST = true;
+    struct Raw { uint32_t d; uint32_t q[8]; };
+    __device__ static void load(Raw &r, const uint8_t *row, int c) {
+        const uint8_t *b = row + 34 * c;
+        r.d = ld_u16(b);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) r.q[i] = ld_u16(b + 2 + 4 * i) | (ld_u16(b + 4 + 4 * i) << 16);
+    }
+    __device__ static void decode(const Raw &r, int c, uint32_t (&o)[16]) {
+        (void)c;
+        const float d = h2f(r.d), cb = -128.0f * d;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t u = r.q[i] ^ 0x80808080u;
+            float w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                w[j] = __fmaf_rn(d, __int_as_float(__byte_perm(u, 0x4B000000u, 0x7650u | (uint32_t)j)) - 8388608.0f, cb);
+            o[2 * i] = pack_bf16x2(w[0], w[1]);
+            o[2 * i + 1] = pack_bf16x2(w[2], w[3]);
+        }
+    }
+};
+
+// BF16 weights: the operand itself (64 bytes per chunk, 16-byte aligned).
+template <> struct Slab<T_BF16> {
+    static constexpr bool FAST = true;
+    struct Raw { uint4 v[4]; };
+    __device__ static void load(Raw &r, const uint8_t *row, int c) {
+        const uint8_t *b = row + 64 * c;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) r.v[i] = ld_u128(b + 16 * i);
+    }
+    __device__ static void decode(const Raw &r, int c, uint32_t (&o)[16]) {
+        (void)c;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            o[4 * i] = r.v[i].x; o[4 * i + 1] = r.v[i].y; o[4 * i + 2] = r.v[i].z; o[4 * i + 3] = r.v[i].w;
+        }
+    }
+};
+
+// F16 weights: each binary16 value (exact in binary32) rounded to bf16, nearest even.
+template <> struct Slab<T_F16> {
+    static constexpr bool FAST = true;
+    struct Raw { uint4 v[4]; };
+    __device__ static void load(Raw &r, const uint8_t *row, int c) {
+        const uint8_t *b = row + 64 * c;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) r.v[i] = ld_u128(b + 16 * i);
+    }
+    __device__ static void decode(const Raw &r, int c, uint32_t (&o)[16]) {
+        (void)c;
+        const uint32_t h[16] = {r.v[0].x, r.v[0].y, r.v[0].z, r.v[0].w, r.v[1].x, r.v[1].y, r.v[1].z, r.v[1].w,
+                                r.v[2].x, r.v[2].y, r.v[2].z, r.v[2].w, r.v[3].x, r.v[3].y, r.v[3].z, r.v[3].w};
+#pragma unroll
+        for (int j = 0; j < 16; ++j) o[j] = pack_bf16x2(h2f(h[j] & 0xffffu), h2f(h[j] >> 16));
+    }
+};
+
 }  // namespace mm
 }  // namespace wqk

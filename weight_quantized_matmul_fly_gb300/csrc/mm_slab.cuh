@@ -296,6 +296,70 @@ template <> struct Slab<T_Q8_0> {
     }
 };
 
+// Q2_K: 84-byte super-blocks (4-byte aligned); chunk t (sub-blocks 2t, 2t+1 of 16) takes 2-bit field g = t & 3
+// of the 32 code bytes at 16 + 32 * (t >> 2), scale bytes 2t and 2t+1 (low nibble scale, high nibble
+// minimum), d and dmin at 80; w = d * sc * q - dmin * mn, computed as fma(ds, q, -dm) (exact, as decoded).
+template <> struct Slab<T_Q2_K> {
+    static constexpr bool FAST = true;
+    struct Raw { uint32_t sm, dd; uint32_t q[8]; };
+    __device__ static void load(Raw &r, const uint8_t *row, int c) {
+        const uint8_t *b = row + 84 * (c >> 3);
+        const int t = c & 7;
+        r.sm = ld_u16(b + 2 * t);
+        r.dd = ld_u32(b + 80);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) r.q[i] = ld_u32(b + 16 + 32 * (t >> 2) + 4 * i);
+    }
+    __device__ static void decode(const Raw &r, int c, uint32_t (&o)[16]) {
+        const int g = c & 3;
+        const float d = h2f(r.dd & 0xffffu), dmin = h2f(r.dd >> 16);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const uint32_t sc = (r.sm >> (8 * half)) & 255u;
+            const float ds = __fmul_rn(d, u2f_small(sc & 15u)), dm = __fmul_rn(dmin, u2f_small(sc >> 4));
+#pragma unroll
+            for (int i = 4 * half; i < 4 * half + 4; ++i)
+                fma4_pack_m((r.q[i] >> (2 * g)) & 0x03030303u, ds, -dm, o[2 * i], o[2 * i + 1]);
+        }
+    }
+};
+
+// Q3_K: 110-byte super-blocks (2-byte aligned): 32 high-bit bytes, 64 low-bit bytes, 12 bytes of 6-bit
+// scales, d. Chunk t: low 2-bit field g = t & 3 of the 32 bytes at 32 + 32 * (t >> 2), high bit t of the
+// high-bit bytes, scales 2t and 2t+1 (offset 32); w = d * (sc - 32) * (q - 4) = ds * (128 + q) - 132 * ds,
+// both terms exact.
+template <> struct Slab<T_Q3_K> {
+    static constexpr bool FAST = true;
+    struct Raw { uint32_t hm[8], q[8]; uint32_t s0, s1, s2, d; };
+    __device__ static void load(Raw &r, const uint8_t *row, int c) {
+        const uint8_t *b = row + 110 * (c >> 3);
+        const int t = c & 7;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            r.hm[i] = ld_u32_a2(b + 4 * i);
+            r.q[i] = ld_u32_a2(b + 32 + 32 * (t >> 2) + 4 * i);
+        }
+        r.s0 = ld_u32_a2(b + 96);
+        r.s1 = ld_u32_a2(b + 100);
+        r.s2 = ld_u32_a2(b + 104);
+        r.d = ld_u16(b + 108);
+    }
+    __device__ static void decode(const Raw &r, int c, uint32_t (&o)[16]) {
+        const int t = c & 7, g = t & 3;
+        const float d = h2f(r.d);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const float ds = __fmul_rn(d, i2f_small((int)six_bits(r.s0, r.s1, r.s2, 2 * t + half) - 32));
+            const float cb = -132.0f * ds;
+#pragma unroll
+            for (int i = 4 * half; i < 4 * half + 4; ++i) {
+                const uint32_t v = ((r.q[i] >> (2 * g)) & 0x03030303u) | (((r.hm[i] >> t) & 0x01010101u) << 2);
+                fma4_pack(v, ds, cb, o[2 * i], o[2 * i + 1]);
+            }
+        }
+    }
+};
+
 // BF16 weights: the operand itself (64 bytes per chunk, 16-byte aligned).
 template <> struct Slab<T_BF16> {
     static constexpr bool FAST = true;

@@ -198,20 +198,22 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (e1 > a0) ptx::prefetch_l2(reinterpret_cast<const void *>(a0), (uint32_t)(e1 - a0));
         }
         if (!early) asm volatile("griddepcontrol.wait;" ::: "memory");
-        // raw bytes of the group's next PF K steps are in flight while a step is decoded (rw[0] is the
-        // step being decoded, rw[PF] the one requested during it)
-        typename SL::Raw rw[PF + 1];
+        // raw bytes of the group's next PFT K steps are in flight while a step is decoded (rw[0] is the
+        // step being decoded, rw[PFT] the one requested during it)
+        constexpr int PFT = pf_of<QT>();
+        typename SL::Raw rw[PFT + 1];
         if constexpr (SL::FAST) {
             const int c0 = 2 * (kbeg + grp) + h;
 #pragma unroll
-            for (int j = 0; j < PF; ++j)
+            for (int j = 0; j < PFT; ++j)
                 if (grp + j * NGRP < nsteps && c0 + 2 * j * NGRP < nchunks) SL::load(rw[j], wrow, c0 + 2 * j * NGRP);
         }
         for (int i = grp; i < nsteps; i += NGRP) {
             const int s = i % STAGES;
             const int c = 2 * (kbeg + i) + h;
             if constexpr (SL::FAST) {
-                if (i + PF * NGRP < nsteps && c + 2 * PF * NGRP < nchunks) SL::load(rw[PF], wrow, c + 2 * PF * NGRP);
+                if (i + PFT * NGRP < nsteps && c + 2 * PFT * NGRP < nchunks)
+                    SL::load(rw[PFT], wrow, c + 2 * PFT * NGRP);
             }
             if (i >= STAGES && !ptx::mbar_wait(&sm->empty[s], ((i / STAGES) - 1) & 1, status)) {
                 sm->abort = 1;
@@ -264,7 +266,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (lane == 0) ptx::mbar_arrive(&sm->full_a[s]);
             if constexpr (SL::FAST) {
 #pragma unroll
-                for (int j = 0; j < PF; ++j) rw[j] = rw[j + 1];
+                for (int j = 0; j < PFT; ++j) rw[j] = rw[j + 1];
             }
         }
     }

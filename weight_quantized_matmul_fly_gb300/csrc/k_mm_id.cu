@@ -26,7 +26,7 @@ using mm::BK;
 using mm::BM;
 using mm::NDEC;
 using mm::NGRP;
-using mm::PF;
+using mm::pf_of;
 using mm::THREADS;
 
 struct Experts {
@@ -221,18 +221,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         bool stop = false;
         for (int p = 0; p < npass && !stop; ++p) {
             const int cnt = ns - p * TN < TN ? ns - p * TN : TN;
-            typename SL::Raw rw[PF + 1];
+            constexpr int PFT = pf_of<QT>();
+            typename SL::Raw rw[PFT + 1];
             if constexpr (SL::FAST) {
                 const int c0 = 2 * grp + h;
 #pragma unroll
-                for (int j = 0; j < PF; ++j)
+                for (int j = 0; j < PFT; ++j)
                     if (grp + j * NGRP < nsteps && c0 + 2 * j * NGRP < nchunks) SL::load(rw[j], wrow, c0 + 2 * j * NGRP);
             }
             for (int i = grp; i < nsteps; i += NGRP) {
                 const int g = p * nsteps + i, s = g % STAGES, xs = g % XSLOTS;
                 const int c = 2 * i + h;
                 if constexpr (SL::FAST) {
-                    if (i + PF * NGRP < nsteps && c + 2 * PF * NGRP < nchunks) SL::load(rw[PF], wrow, c + 2 * PF * NGRP);
+                    if (i + PFT * NGRP < nsteps && c + 2 * PFT * NGRP < nchunks)
+                        SL::load(rw[PFT], wrow, c + 2 * PFT * NGRP);
                 }
                 if (g >= STAGES && !ptx::mbar_wait(&sm->empty[s], ((g / STAGES) - 1) & 1, status)) {
                     sm->abort = 1;
@@ -293,7 +295,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (lane == 0) ptx::mbar_arrive(&sm->full_a[s]);
                 if constexpr (SL::FAST) {
 #pragma unroll
-                    for (int j = 0; j < PF; ++j) rw[j] = rw[j + 1];
+                    for (int j = 0; j < PFT; ++j) rw[j] = rw[j + 1];
                 }
             }
             stop = !__all_sync(0xffffffffu, !stop);

@@ -16,6 +16,8 @@ constexpr int BM = 128;            // weight rows per CTA
 constexpr int BK = 64;             // columns per K step: one 128-byte swizzle row of bf16
 constexpr int MAX_STAGES = 8;
 constexpr int PF = 2;              // K steps of its own group a decoder warp keeps in flight (raw bytes in registers)
+// ... per weight type: one for F32, whose 32-weight chunk is 128 bytes
+template <int QT> __host__ __device__ constexpr int pf_of() { return QT == T_F32 ? 1 : PF; }
 constexpr int A_STAGE = BM * BK * 2;   // 16 KB
 constexpr int NDEC = 16;               // decoder / epilogue warps: two groups of 8 taking alternate K steps
 constexpr int NGRP = NDEC / 8;         // decoder groups (one slab = 8 warps x 16 rows)
@@ -356,6 +358,26 @@ template <> struct Slab<T_Q3_K> {
                 const uint32_t v = ((r.q[i] >> (2 * g)) & 0x03030303u) | (((r.hm[i] >> t) & 0x01010101u) << 2);
                 fma4_pack(v, ds, cb, o[2 * i], o[2 * i + 1]);
             }
+        }
+    }
+};
+
+// F32 weights: each value rounded to bf16, nearest even (128 bytes per chunk, 16-byte aligned). The raw
+// buffer is 32 registers, so this type keeps one K step in flight instead of PF (pf_of).
+template <> struct Slab<T_F32> {
+    static constexpr bool FAST = true;
+    struct Raw { uint4 v[8]; };
+    __device__ static void load(Raw &r, const uint8_t *row, int c) {
+        const uint8_t *b = row + 128 * c;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) r.v[i] = ld_u128(b + 16 * i);
+    }
+    __device__ static void decode(const Raw &r, int c, uint32_t (&o)[16]) {
+        (void)c;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            o[2 * i] = pack_bf16x2(__uint_as_float(r.v[i].x), __uint_as_float(r.v[i].y));
+            o[2 * i + 1] = pack_bf16x2(__uint_as_float(r.v[i].z), __uint_as_float(r.v[i].w));
         }
     }
 };

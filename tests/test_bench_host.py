@@ -1,4 +1,4 @@
-"""Host-side arithmetic of bench.py (no GPU): the per-call roofline of the survey's measurement rule,
+"""Host-side arithmetic of bench.py (no GPU): the per-call roofline of the measurement rule,
 max((weight + activation bytes) / HBM, 2 M N K / bf16 peak), and its per-class sums."""
 import os
 import sys
@@ -36,3 +36,17 @@ def test_reference_arm_reports_the_same_config():
     assert bench.bench_config(1) == bench.bench_config(1)
     c = bench.bench_config(1)
     assert c["calls_per_step"] == 105 and "workload" in c
+
+
+def test_recorded_traffic_only_for_its_class_and_sources(monkeypatch):
+    """The roofline's DRAM traffic is reported for the recorded class while the kernel and planner sources
+    hash to the recorded digest, and is withheld once any of them differs."""
+    rec = dict(bench.TRAFFIC)
+    monkeypatch.setattr(bench, "TRAFFIC", dict(rec, sha256=bench.sources_digest(rec["sources"])))
+    got = bench.recorded_traffic(rec["class"])
+    assert got is not None and got["bytes_per_call"] == rec["bytes_per_call"]
+    assert got["bytes_per_call"] >= got["algorithmic_bytes_per_call"] > 0
+    assert bench.recorded_traffic("m_le_16" if rec["class"] != "m_le_16" else "m_ge_512") is None
+    monkeypatch.setattr(bench, "TRAFFIC", dict(rec, sha256="0" * 64))
+    assert bench.recorded_traffic(rec["class"]) is None
+

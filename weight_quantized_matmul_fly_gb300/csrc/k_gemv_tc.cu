@@ -1299,6 +1299,14 @@ int launch_gtc_t(const MatSet &ms, int64_t K, const void *x, int M, unsigned int
     // resident tiles (measured: ffn_down 2560x9728 Q6_K at 7 tokens 25.6 us as a ring); for matrices
     // up to 64 MB the caller halves the tokens instead.
     if (NT > 1 && best_ns > 0 && total_rows * row_bytes(QT, K) < ((int64_t)64 << 20)) return -3;
+    // 9-16 binary32 tokens (hi + lo: 32 MMA columns) stage as many activation bytes per K as the tile holds
+    // weight bytes, so no split of a large matrix fits two CTAs per SM; for the 2-5-bit types two launches
+    // of up to 8 tokens, the second finding the weights in L2, measured faster there (9728 x 2560 at 16
+    // tokens: Q4_K 31.3 -> 23.2 us, Q4_0 28.6 -> 20.6, Q2_K 29.8 -> 23.8, Q5_0 32.2 -> 27.7), and slower for
+    // Q3_K, Q6_K and Q8_0, which stay one launch, as do small matrices.
+    constexpr bool kHalve16 = QT == T_Q4_0 || QT == T_Q4_1 || QT == T_Q5_0 || QT == T_Q5_1 || QT == T_Q2_K ||
+                              QT == T_Q4_K || QT == T_Q5_K;
+    if (kHalve16 && NT == 4 && !XBF16 && total_rows * K >= ((int64_t)16 << 20)) return -3;
     if (dry) return 0;                                                // planning only (launch counting)
     const int64_t kseg = ((nmacro + best_s - 1) / best_s) * 256;
     if constexpr (KWMAX >= 8) if (best_kw == 8) return launch_gtc_kw<QT, NT, XBF16, 8>(ms, K, x, M, best_s, kseg, best_ns, status, st, stall, early);

@@ -95,8 +95,10 @@ enum qmm_type {
  * path rounds x and the dequantized weights to bfloat16 (round to nearest even) and accumulates in
  * binary32 (for Q4_K, Q5_K and A4G64 the weight rounded is the binary32 weight up to 2^-17 times its
  * sub-block scale); the mat-vec path multiplies the binary32 dequantized weights by x in binary32.
- * qmm() allocates nothing and launches one kernel per call on either path. Its work plan (a function of
- * the type, N, K and M) may split the K dimension over S <= 8 thread blocks; they form a cluster and add
+ * qmm() allocates nothing. It launches one kernel on the tensor-core path, and on the mat-vec path one per
+ * group of tokens (all of them, or two halves where a group's activations do not fit on chip next to its
+ * weights, and for 9-16 binary32 tokens of large 2-5-bit matrices; see qmm_launch_count). On the
+ * tensor-core path the work plan (a function of the type, N, K and M) may split the K dimension over S <= 8 thread blocks; they form a cluster and add
  * their partial sums in split order in shared memory. Binary32 activations are rounded to bfloat16 inside
  * the tensor-core kernel, with at most 128 token columns per thread block. qmm_ws() is faster on that
  * path with binary32 activations and M > 32: with scratch (qmm_workspace_size()), a separate pass writes a

@@ -99,8 +99,9 @@ enum qmm_type {
  * group of tokens (all of them, or two halves where a group's activations do not fit on chip next to its
  * weights, and for 9-16 binary32 tokens of large 2-5-bit matrices; see qmm_launch_count). On the
  * tensor-core path the work plan (a function of the type, N, K and M) may split the K dimension over
- * S <= 8 thread blocks; they form a cluster and add their partial sums in split order in shared memory. Binary32 activations are rounded to bfloat16 inside
- * the tensor-core kernel, with at most 128 token columns per thread block. qmm_ws() is faster on that
+ * S <= 8 thread blocks; they form a cluster and add their partial sums in split order in shared memory.
+ * Binary32 activations are rounded to bfloat16 inside the tensor-core kernel, with at most 128 token
+ * columns per thread block. qmm_ws() is faster on that
  * path with binary32 activations and M > 32: with scratch (qmm_workspace_size()), a separate pass writes a
  * bfloat16 copy of x that the kernel reads at the plan's full width, and a K split (up to 32 thread blocks)
  * sends its partial sums through the scratch to a second kernel that adds them in split order. The two

@@ -101,12 +101,11 @@ enum qmm_type {
  * tensor-core path the work plan (a function of the type, N, K and M) may split the K dimension over
  * S <= 8 thread blocks; they form a cluster and add their partial sums in split order in shared memory.
  * Binary32 activations are rounded to bfloat16 inside the tensor-core kernel, with at most 128 token
- * columns per thread block. qmm_ws() is faster on that
- * path with binary32 activations and M > 32: with scratch (qmm_workspace_size()), a separate pass writes a
- * bfloat16 copy of x that the kernel reads at the plan's full width, and a K split (up to 32 thread blocks)
- * sends its partial sums through the scratch to a second kernel that adds them in split order. The two
- * plan their K split separately, so their results can differ in the last bits (both within the stated
- * tolerance); each is bit-identical across token tiles.
+ * columns per thread block. qmm_ws() is faster on that path with binary32 activations and M > 32: with
+ * scratch (qmm_workspace_size()), a separate pass writes a bfloat16 copy of x that the kernel reads at the
+ * plan's full width, and a K split (up to 32 thread blocks) sends its partial sums through the scratch to
+ * a second kernel that adds them in split order. The two plan their K split separately, so their results
+ * can differ in the last bits (both within the stated tolerance); each is bit-identical across token tiles.
  */
 int qmm(const void *wq, int qtype, int64_t N, int64_t K, const void *x, int64_t M, float *y, void *stream);
 

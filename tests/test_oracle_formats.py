@@ -6,7 +6,8 @@ field writer (tests/spec_fields.py, written from the specification's layout tabl
 oracle's C) and compared exactly as rationals.
 
 Encoder: round-trip bound of the specification's section 4 on several weight distributions, read back with
-the tests' own field reader; codes and sub-scales in range.
+the tests' own field reader; codes and sub-scales in range; literal blocks whose scale and codes follow from
+the section's rules by hand.
 """
 import zlib
 from fractions import Fraction
@@ -263,3 +264,37 @@ def test_encoder_error_scale(orc, qtype):
     limit = {"Q8_0": 0.01, "Q6_K": 0.02, "Q5_0": 0.06, "Q5_1": 0.05, "Q5_K": 0.06, "Q4_0": 0.12,
              "Q4_1": 0.10, "Q4_K": 0.12, "A4G64": 0.12, "Q3_K": 0.30, "Q2_K": 0.60}[qtype]
     assert rel < limit, rel
+
+
+# ---------------------------------------------------------------- encoder: literal decisions
+# Blocks whose scale and codes follow from the specification's section 4 by hand (every quotient below is
+# exact, and the ties go to even), so that a different scale rule (say amax / 8 for Q4_0) or a tie rounded
+# away from zero changes the bytes.
+
+def test_encoder_q4_0_literal(orc):
+    # amax = 7 -> d = f16(7 / 7) = 1.0 (0x3C00); q = rne(w) + 8 (3.5 -> 4, 2.5 -> 2, -2.5 -> -2, -0.5 -> 0)
+    w = np.zeros(32, dtype=np.float32)
+    w[:8] = [7.0, -7.0, 3.5, 2.5, 1.5, 0.5, -0.5, -1.5]
+    w[16:20] = [-7.0, 6.0, -2.5, 0.25]
+    codes = [15, 1, 12, 10, 10, 8, 8, 6] + [8] * 8 + [1, 14, 6, 8] + [8] * 12
+    want = bytes([0x00, 0x3C]) + bytes(codes[j] | (codes[j + 16] << 4) for j in range(16))
+    assert orc.quantize("Q4_0", w.reshape(1, 32)).tobytes() == want
+
+
+def test_encoder_q8_0_literal(orc):
+    # amax = 127 -> d = f16(127 / 127) = 1.0; q = rne(w): 63.5 -> 64, 62.5 -> 62, -0.5 -> 0
+    w = np.zeros(32, dtype=np.float32)
+    w[:6] = [127.0, -127.0, 63.5, 62.5, -0.5, 1.25]
+    codes = [127, -127, 64, 62, 0, 1] + [0] * 26
+    want = bytes([0x00, 0x3C]) + bytes(c & 0xFF for c in codes)
+    assert orc.quantize("Q8_0", w.reshape(1, 32)).tobytes() == want
+
+
+def test_encoder_q4_1_literal(orc):
+    # lo = -2, hi = 13 -> d = f16(15 / 15) = 1.0, m = f16(-2) (0xC000); q = rne(w + 2): 0.5 -> 2.5 -> 2,
+    # 1.5 -> 3.5 -> 4, -2 -> 0, 13 -> 15
+    w = np.full(32, 3.0, dtype=np.float32)
+    w[:4] = [-2.0, 13.0, 0.5, 1.5]
+    codes = [0, 15, 2, 4] + [5] * 28
+    want = bytes([0x00, 0x3C, 0x00, 0xC0]) + bytes(codes[j] | (codes[j + 16] << 4) for j in range(16))
+    assert orc.quantize("Q4_1", w.reshape(1, 32)).tobytes() == want
